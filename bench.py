@@ -1,0 +1,387 @@
+"""Benchmark of the fused tree-verify step (lbx_verify_step) on GB300.
+
+Default workload: the full verify step of a 27B-class hybrid target -- 48
+gated-DeltaNet layers, 16 key / 48 value heads, d = 128, conv width 4, one
+request, a 22-node DDTree draft tree (budget 22).  One step = one call of
+lbx_verify_step over all layers (conv + recurrence + persist).
+
+Prints one JSON line.  `value` is node-head updates per second (L*Bq*N*Hv per
+step) with inputs resident in HBM; `e2e` is the same metric through the C ABI
+with the step's inputs copied from pinned host memory and o copied back inside
+the timed region.  `--impl reference` times the fp64 CPU oracle instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lbx|reference]
+                       [--workload NAME]
+Under torchrun each rank runs an independent replica (the path needs no
+exchange between GPUs); value is the sum over ranks of the work done divided
+by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tree_verify_linear_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "µs per DDTree verify step & node-head updates/s; HBM GB/s vs ~8 TB/s roofline"
+UNIT = "node-head updates/s"
+KERNEL = "gdn_step_kernel"
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one fused step must move at minimum: state and conv window read
+    and written once per (layer, request), conv weights once per layer, the
+    bf16 inputs and gates, the tree indices (parent, slot, accepted) and o."""
+    C = w.C
+    per_lb = (2 * w.Hv * w.d * w.d * 4          # state read + write
+              + 2 * (w.K - 1) * C * 4           # conv window read + write
+              + w.N * C * 2                     # x
+              + 2 * w.N * w.Hv * 2              # a, b
+              + (w.N + 2) * 4                   # parent, slot, accepted
+              + w.N * w.Hv * w.d * 4)           # o
+    return w.L * (w.Bq * per_lb + C * w.K * 2)  # conv_w once per layer
+
+
+def describe(w) -> str:
+    tree = {"ddtree": f"budget-{w.N} DDTree-shaped tree", "uniform": f"{w.N}-node uniform tree",
+            "chain": f"{w.N}-token chain"}[w.tree]
+    return (f"{w.name}: {w.L} GDN layers, {w.Bq} request(s), {tree}, Hk={w.Hk}, Hv={w.Hv}, "
+            f"d={w.d}, conv width {w.K}")
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tree_verify_linear_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [r for t, r in self.rows if self.t_on and self.t_off and self.t_on <= t <= self.t_off]
+        if not rows:
+            rows = [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 4 + i and r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("LBX_BENCH_GLOO") is None else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline and the reference arm).
+# ---------------------------------------------------------------------------
+def oracle_rate(w, inp, budget_s: float, n_threads: int = 0):
+    """Time the fp64 oracle (full verify step: conv, recurrence, accepted
+    state) on whole (layer, request) slices until about budget_s seconds of
+    work; returns (updates/s, threads, description)."""
+    import oracle
+    oracle.lib()
+    done_heads = 0
+    used = 1
+    t0 = time.perf_counter()
+    slices = [(l, b) for l in range(w.L) for b in range(w.Bq)]
+    for (l, b) in slices:
+        items = [(l, b, h) for h in range(w.Hv)]
+        _, _, used = oracle.verify_heads(w, inp, items, n_threads=n_threads)
+        done_heads += len(items)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    rate = done_heads * w.N / dt
+    n_slices = done_heads // w.Hv
+    return rate, used, f"{n_slices} of {len(slices)} (layer, request) slices, all {w.Hv} heads"
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    inp = make_inputs(w)
+    items_all = [(l, b, h) for l in range(w.L) for b in range(w.Bq) for h in range(w.Hv)]
+    # size each step so the whole run takes about a minute
+    t = time.perf_counter()
+    _, _, used = oracle.verify_heads(w, inp, items_all[:w.Hv])
+    per_head = (time.perf_counter() - t) / w.Hv
+    total = args.steps + args.warmup
+    heads_per_step = int(max(1, min(len(items_all), 60.0 / max(total, 1) / max(per_head, 1e-9))))
+    k = 0
+    times = []
+    for s in range(total):
+        items = [items_all[(k + i) % len(items_all)] for i in range(heads_per_step)]
+        k += heads_per_step
+        t = time.perf_counter()
+        _, _, used = oracle.verify_heads(w, inp, items)
+        dt = time.perf_counter() - t
+        if s >= args.warmup:
+            times.append(dt)
+    sec = sum(times)
+    value = heads_per_step * w.N * len(times) / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"each step: {heads_per_step} (layer, request, head) items of "
+                                   f"the workload, full conv + recurrence + accepted state"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm.
+# ---------------------------------------------------------------------------
+def run_lbx(args, w):
+    import torch
+    from tree_verify_linear_gb300 import lbx
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lbx.load()
+    inp = make_inputs(w, seed=w.seed + 7919 * rank)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = {k: to_dev(v) for k, v in inp.items()}
+    cfg = lbx.cfg_of(w)
+    o = torch.empty((w.L, w.Bq, w.N, w.Hv, w.d), device=dev)
+    ws = lbx.new_workspace(cfg, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lbx.lbx_verify_step(cfg, d["x"], d["conv_w"], d["a"], d["b"], d["parent"], d["slot"],
+                            d["accepted"], d["state"], d["conv_cache"], o, ws, status, stream)
+
+    # ---- device-resident timing ----
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    gpu_id = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid) if uuid else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    ms_local = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms_local, world, dev)
+    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    units = w.L * w.Bq * w.N * w.Hv
+    value = units * args.steps * world / (ms / 1e3)
+    ms_per_step = ms / args.steps
+
+    # ---- end to end: host buffers through the C ABI ----
+    names_in = ("x", "a", "b", "parent", "slot", "accepted")
+    host = {k: d[k].cpu().pin_memory() for k in names_in}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        for k in names_in:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = units * e2e_steps * world / (e2e_ms / 1e3)
+
+    if rank != 0:
+        return
+
+    peak, peak_kind = read_peaks()
+    alg = algorithmic_bytes(w)
+    achieved = alg / (ms_per_step / 1e3) / 1e9
+    traffic = recorded_traffic(w.name)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, cores, sample = oracle_rate(w, inp, budget_s=args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "L": w.L, "Bq": w.Bq, "N": w.N, "Hk": w.Hk,
+                   "Hv": w.Hv, "d": w.d, "K": w.K, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({alg / 1e6:.1f} MB moved per step)"},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": alg, "kernel": KERNEL},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("lbx", "reference"), default="lbx")
+    ap.add_argument("--workload", default="step27b", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_lbx(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * lbx.h -- C ABI of the tree-verify gated-DeltaNet library (GB300, sm_103a).
+ *
+ * The library computes the verify step of a hybrid model's gated-DeltaNet
+ * (linear-attention) layers for a DDTree draft tree: the three tree-aware
+ * state-rollback operations named in the Lucebox hub README (section
+ * "02 DFlash DDtree", list "Implemented here": ggml_ssm_conv_tree,
+ * ggml_gated_delta_net_tree, ggml_gated_delta_net_tree_persist), plus one
+ * fused entry point that performs all three in a single pass.  DDTree itself
+ * (same section, "Algorithms used") is a tree-structured verify: the draft is
+ * a tree of B nodes given as a parent-index array, and every node is verified
+ * against the state reached along its own root-to-node path.
+ *
+ * Notation.  L layers, Bq requests, N tree nodes (the budget), Hk key heads,
+ * Hv value heads (Hv % Hk == 0; value head h reads key head h / (Hv/Hk)),
+ * d = d_k = d_v, K conv width, C = 2*Hk*d + Hv*d conv channels ordered
+ * q | k | v.  For each layer, request and value head h the recurrence is the
+ * gated delta rule
+ *     S_n = a_n S_p (I - b_n k_n k_n^T) + b_n v_n k_n^T,   o_n = q_scale * S_n q_n,
+ * where p = parent[n] and S_p of the root (node 0) is the cached state of the
+ * request's slot.  S is d_v x d_k, stored row-major [d_v][d_k].
+ *
+ * Conventions shared by every entry point:
+ *   - Every array pointer is a DEVICE pointer owned by the caller; the
+ *     library allocates nothing.  bf16 values are passed as their 16-bit
+ *     patterns (uint16_t).  All arrays are dense and row-major in the index
+ *     order written next to them; each must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream`.  The return value reports host-side
+ *     argument checks and the launch: LBX_OK, LBX_EINVAL or LBX_ECUDA.
+ *   - Structural errors that only the device can see (a parent array that is
+ *     not a topologically numbered tree, a slot or accepted index out of
+ *     range, two requests naming the same slot, a chain-mode input that is
+ *     not a chain) are reported through `d_status` (an int32 in device memory,
+ *     may be NULL): the kernel stores LBX_ETREE or LBX_EINVAL there and then
+ *     writes NOTHING -- no outputs, no cache update.  `d_status` is never
+ *     cleared by the library; zero it before the call to read it afterwards.
+ *   - The draft tree: parent[b][0] == -1 (node 0 is the root, the last
+ *     accepted token), and 0 <= parent[b][i] < i for i > 0.  One tree per
+ *     request is shared by all layers.
+ *   - Caches: state[L][n_slots][Hv][d][d] fp32 and conv_cache[L][n_slots][K-1][C]
+ *     fp32 (raw pre-conv inputs, oldest row first; with K == 1 there is no
+ *     conv cache and its pointer may be NULL).  Request b uses slot
+ *     slot[b]; slots that no request names are never read or written.
+ */
+#ifndef LBX_H
+#define LBX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define LBX_OK 0
+#define LBX_EINVAL (-1) /* bad dimension, NULL pointer, size over a limit   */
+#define LBX_ECUDA (-2)  /* a CUDA call or kernel launch failed               */
+#define LBX_ETREE (-3)  /* invalid tree (device-detected, via d_status)      */
+
+/* Limits. */
+#define LBX_MAX_TREE_NODES 64 /* tree mode: N <= 64 nodes per request          */
+#define LBX_CHAIN_CHUNK 64    /* chunked (chain) mode processes 64 tokens/chunk */
+#define LBX_MAX_CONV_WIDTH 4  /* 1 <= K <= 4                                    */
+
+/* Modes of lbx_verify_step. */
+#define LBX_MODE_AUTO 0    /* tree if N <= LBX_MAX_TREE_NODES, else chunked     */
+#define LBX_MODE_TREE 1    /* arbitrary tree, N <= LBX_MAX_TREE_NODES           */
+#define LBX_MODE_CHUNKED 2 /* chain only (parent[i] == i-1), any N >= 1         */
+
+typedef struct lbx_cfg {
+  int L;       /* gated-DeltaNet layers in the call (>= 1)                     */
+  int Bq;      /* requests (>= 1)                                              */
+  int N;       /* tree nodes per request (>= 1)                                */
+  int Hk, Hv;  /* key / value heads, Hv % Hk == 0                              */
+  int d;       /* head dimension d_k = d_v; 32 or 128                          */
+  int K;       /* conv width, 1..LBX_MAX_CONV_WIDTH                            */
+  int n_slots; /* cache slots in state / conv_cache (>= Bq)                    */
+  float l2_eps;  /* q, k <- x / sqrt(sum x^2 + l2_eps); typical 1e-6           */
+  float q_scale; /* o_n = q_scale * S_n q_n; 1.0 for the plain recurrence      */
+  int mode;      /* LBX_MODE_*; used by lbx_verify_step only                   */
+} lbx_cfg;
+
+/* Human-readable text for a status code (static storage). */
+const char *lbx_strerror(int status);
+
+/* Bytes of workspace lbx_verify_step needs for cfg (0 on a bad cfg).  The
+ * workspace holds one arrival counter per (layer, request, key head); it must
+ * be zero-filled once before its first use, and every call that runs to
+ * completion leaves it zero again.  Two calls that run at the same time must
+ * not share a workspace. */
+size_t lbx_workspace_size(const lbx_cfg *cfg);
+
+/*
+ * Tree conv (ggml_ssm_conv_tree; Lucebox hub README, "02 DFlash DDtree").
+ * For node n and channel c:
+ *     y = sum_{j=0}^{K-1} conv_w[l][c][K-1-j] * xhat_j[c],   out = y * sigmoid(y)
+ * where xhat_0 is node n's input, xhat_1 its parent's, and so on up the
+ * ancestor path; past the root the window continues into the slot's conv
+ * cache, most recent cached row first.  Then q and k are L2-normalised per
+ * key head over d channels (v is not).
+ *   x          [L][Bq][N][C]   bf16   raw inputs of the tree nodes
+ *   conv_w     [L][C][K]       bf16   depthwise conv weights, no bias
+ *   conv_cache [L][n_slots][K-1][C] fp32 (read only here)
+ *   parent     [Bq][N] int32, slot [Bq] int32
+ *   qkv_out    [L][Bq][N][C]   fp32   (q scaled by nothing; q_scale is applied
+ *                                      by lbx_tree_deltanet)
+ * Requires cfg->N <= LBX_MAX_TREE_NODES.
+ */
+int lbx_tree_conv(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_w,
+                  const float *conv_cache, const int32_t *parent, const int32_t *slot,
+                  float *qkv_out, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * Tree gated delta-rule recurrence (ggml_gated_delta_net_tree; same page).
+ * Every node's state is the recurrence along its root-to-node path, started
+ * from state[l][slot[b]][h]; o_n = q_scale * S_n q_n.
+ *   qkv         [L][Bq][N][C]          fp32 (output of lbx_tree_conv)
+ *   a, b        [L][Bq][N][Hv]         bf16 gates, already activated
+ *   state       [L][n_slots][Hv][d][d] fp32 (read only here)
+ *   parent      [Bq][N], slot [Bq]     int32
+ *   o           [L][Bq][N][Hv][d]      fp32
+ *   node_states [L][Bq][N][Hv][d][d]   fp32 per-node snapshots for a later
+ *                                      lbx_tree_persist; may be NULL
+ * Requires cfg->N <= LBX_MAX_TREE_NODES.
+ */
+int lbx_tree_deltanet(const lbx_cfg *cfg, const float *qkv, const uint16_t *a, const uint16_t *b,
+                      const float *state, const int32_t *parent, const int32_t *slot, float *o,
+                      float *node_states, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * Persist (ggml_gated_delta_net_tree_persist; same page, "state rollback").
+ * For each layer l and request b, with acc = accepted[b]:
+ *   state[l][slot[b]]      <- node_states[l][b][acc]          (all Hv heads)
+ *   conv_cache[l][slot[b]] <- the last K-1 entries of
+ *                             [old cache rows, x of the path root..acc]
+ * Both caches are updated in place.  The conv part copies bf16-exact values
+ * and is bit-exact.
+ *   x           [L][Bq][N][C] bf16, node_states [L][Bq][N][Hv][d][d] fp32,
+ *   parent [Bq][N], slot [Bq], accepted [Bq] int32.
+ */
+int lbx_tree_persist(const lbx_cfg *cfg, const uint16_t *x, const float *node_states,
+                     const int32_t *parent, const int32_t *slot, const int32_t *accepted,
+                     float *state, float *conv_cache, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * Fused verify step: tree conv + tree recurrence + persist in one pass.  The
+ * cached state is read once, per-node states are never materialised, o is
+ * written for every node, and only the accepted node's state and conv window
+ * are written back (in place) to each request's slot.
+ *   x [L][Bq][N][C], conv_w [L][C][K], a, b [L][Bq][N][Hv]   bf16
+ *   parent [Bq][N], slot [Bq], accepted [Bq]                 int32
+ *   state [L][n_slots][Hv][d][d], conv_cache [L][n_slots][K-1][C]  fp32, in/out
+ *   o [L][Bq][N][Hv][d]                                     fp32, out
+ *   workspace / workspace_bytes: >= lbx_workspace_size(cfg) bytes (see there)
+ * Modes: in tree mode N <= LBX_MAX_TREE_NODES; chunked mode takes a chain of
+ * any length and processes it LBX_CHAIN_CHUNK tokens at a time.  Distinct
+ * requests must name distinct slots.
+ */
+int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_w,
+                    const uint16_t *a, const uint16_t *b, const int32_t *parent,
+                    const int32_t *slot, const int32_t *accepted, float *state, float *conv_cache,
+                    float *o, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                    cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LBX_H */

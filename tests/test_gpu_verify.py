@@ -1,0 +1,230 @@
+"""GPU parity of the fused verify step (lbx_verify_step) against the fp64
+oracle, on the seeded workloads at full size and on edge cases.  Calls go
+through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+
+import oracle
+from tree_verify_linear_gb300 import lbx
+from tree_verify_linear_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_inputs
+
+from gpu_util import O_TOL, STATE_TOL, check_verify, run_verify
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    from tree_verify_linear_gb300 import build
+    build.build()
+    lbx.load()
+    oracle.lib()
+
+
+def test_tiny_all_heads():
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w)
+    o, st, cc, status, ws = run_verify(w, inp)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+    assert not ws.any(), "workspace counters must be left at zero"
+
+
+def test_layer27b_all_heads():
+    w = WORKLOADS["layer27b"]
+    inp = make_inputs(w)
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+
+
+def test_step27b_all_heads_full_size():
+    """The 48-layer budget-22 step, every head checked (the bench workload)."""
+    w = WORKLOADS["step27b"]
+    inp = make_inputs(w)
+    o, st, cc, status, ws = run_verify(w, inp)
+    assert status == 0
+    assert np.isfinite(o).all()
+    check_verify(w, inp, o, st, cc)
+    assert not ws.any()
+
+
+def test_serve27b_b22_all_heads_permuted_slots():
+    w = WORKLOADS["serve27b_b22"]
+    inp = make_inputs(w, slots=np.array([4, 0, 6, 2, 1], dtype=np.int32))
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+
+
+def test_serve27b_b64_sampled_layers():
+    w = WORKLOADS["serve27b_b64"]
+    inp = make_inputs(w)
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == 0
+    assert np.isfinite(o).all()
+    items = [(l, b, h) for l in (0, 17, 47) for b in range(w.Bq) for h in range(w.Hv)]
+    check_verify(w, inp, o, st, cc, items=items)
+
+
+def test_chain08b_sampled_heads_chunked():
+    """4096-token chain, 18 layers, chunked mode, against the sequential
+    recurrence of the oracle on a sample of heads (all o of those heads)."""
+    w = WORKLOADS["chain08b"]
+    inp = make_inputs(w)
+    o, st, cc, status, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
+    assert status == 0
+    assert np.isfinite(o).all()
+    rng = np.random.default_rng(0)
+    items = sorted({(int(l), 0, int(h)) for l, h in zip(rng.integers(0, w.L, 12),
+                                                        rng.integers(0, w.Hv, 12))})
+    items += [(w.L - 1, 0, w.Hv - 1), (0, 0, 0)]
+    check_verify(w, inp, o, st, cc, items=items, form=oracle.FORM_SEQUENTIAL)
+
+
+def small(**kw):
+    base = dict(name="edge", L=2, Bq=2, N=13, Hk=2, Hv=4, d=32, tree="uniform",
+                accepted="node", seed=500)
+    base.update(kw)
+    return Workload(**base)
+
+
+EDGE = {
+    "root_only": small(N=1),
+    "two_nodes": small(N=2),
+    "ragged_13": small(N=13),
+    "deep_uniform_64": small(N=64, seed=501),
+    "ddtree_37_d128": small(N=37, Hk=2, Hv=6, d=128, tree="ddtree", seed=502),
+    "d64": small(d=64, N=22, tree="ddtree", seed=503),
+    "conv_k3": small(K=3, seed=504),
+    "conv_k2": small(K=2, seed=505),
+    "conv_k1": small(K=1, seed=506),
+    "q_scale": small(q_scale=float(1 / np.sqrt(32)), seed=507),
+    "gqa_1to1": small(Hk=4, Hv=4, seed=508),
+    "three_requests": small(Bq=3, N=9, tree="ddtree", seed=509),
+    "leaf_accepted": small(accepted="leaf", seed=510),
+    "chain_tree_mode": small(N=64, tree="chain", accepted="last", seed=511),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(name):
+    w = EDGE[name]
+    slots = None
+    if w.Bq == 3:
+        slots = np.array([2, 0, 4], dtype=np.int32)
+    inp = make_inputs(w, slots=slots)
+    o, st, cc, status, ws = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+    assert not ws.any()
+
+
+@pytest.mark.parametrize("N,acc", [(64, 63), (100, 99), (100, 70), (130, 5), (7, 3)])
+def test_chunked_chain_lengths(N, acc):
+    """Chains processed in 64-token chunks, ragged last chunk, accepted node
+    anywhere along the chain (its state is captured mid-chain)."""
+    w = small(N=N, tree="chain", accepted="last", d=128, Hk=2, Hv=2, seed=600 + N)
+    inp = make_inputs(w)
+    inp["accepted"][:] = acc
+    o, st, cc, status, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
+    assert status == 0
+    check_verify(w, inp, o, st, cc, form=oracle.FORM_SEQUENTIAL)
+
+
+def test_tree_and_chunked_modes_agree_on_a_chain():
+    w = small(N=64, tree="chain", accepted="last", d=128, Hk=2, Hv=4, seed=700)
+    inp = make_inputs(w)
+    o1, s1, c1, st1, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
+    o2, s2, c2, st2, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
+    assert st1 == st2 == 0
+    assert np.abs(o1 - o2).max() <= 1e-5 * np.abs(o1).max()
+    assert c1.tobytes() == c2.tobytes()
+
+
+def test_identity_gates_keep_state_and_read_out_S0_q():
+    """a = 1, b = 0: the persisted state equals the cached state and
+    o_n = S0 q_n."""
+    w = small(seed=800)
+    inp = make_inputs(w)
+    inp["a"][...] = bf16_bits(np.ones(inp["a"].shape, np.float32))
+    inp["b"][...] = 0
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+    for l in range(w.L):
+        for b in range(w.Bq):
+            s = inp["slot"][b]
+            d = st[l, s].astype(np.float64) - inp["state"][l, s]
+            assert np.abs(d).max() <= 1e-6 * np.abs(inp["state"][l, s]).max()
+
+
+def test_two_consecutive_steps_match_oracle_twice():
+    """The caches updated in place by one step feed the next; the workspace
+    counters reset themselves in between."""
+    w = WORKLOADS["serve27b_b22"].replace(L=4)
+    inp = make_inputs(w)
+    o, st, cc, status, ws = run_verify(w, inp, steps=2)
+    assert status == 0 and not ws.any()
+    # oracle: two steps in sequence on the same inputs
+    _, s1, c1 = oracle.verify_step_full(w, inp)
+    inp2 = dict(inp)
+    inp2["state"] = inp["state"].copy()
+    for b in range(w.Bq):
+        inp2["state"][:, inp["slot"][b]] = s1[:, inp["slot"][b]].astype(np.float32)
+    inp2["conv_cache"] = c1
+    check_verify(w, inp2, o, st, cc)
+
+
+# -------------------------------------------------------------------------
+# Errors the device detects: status is set and nothing is written.
+# -------------------------------------------------------------------------
+def _assert_untouched(inp, o, st, cc):
+    assert st.tobytes() == inp["state"].tobytes()
+    assert cc.tobytes() == inp["conv_cache"].tobytes()
+    assert np.isnan(o).all()
+
+
+@pytest.mark.parametrize("bad", ["root_parent", "forward_parent", "out_of_range"])
+def test_invalid_tree_sets_status_and_writes_nothing(bad):
+    w = small(seed=900)
+    inp = make_inputs(w)
+    if bad == "root_parent":
+        inp["parent"][1, 0] = 0
+    elif bad == "forward_parent":
+        inp["parent"][0, 5] = 7
+    else:
+        inp["parent"][1, 3] = 99
+    o, st, cc, status, ws = run_verify(w, inp)
+    assert status == lbx.LBX_ETREE
+    _assert_untouched(inp, o, st, cc)
+    assert not ws.any()
+
+
+def test_duplicate_slots_and_bad_accepted_rejected_on_device():
+    w = small(seed=901)
+    inp = make_inputs(w, slots=np.array([1, 1], dtype=np.int32))
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == lbx.LBX_EINVAL
+    _assert_untouched(inp, o, st, cc)
+    inp = make_inputs(w)
+    inp["accepted"][1] = w.N
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == lbx.LBX_EINVAL
+    _assert_untouched(inp, o, st, cc)
+    inp = make_inputs(w)
+    inp["slot"][0] = w.n_slots
+    o, st, cc, status, _ = run_verify(w, inp)
+    assert status == lbx.LBX_EINVAL
+
+
+def test_chunked_mode_rejects_a_non_chain():
+    w = small(N=80, tree="chain", accepted="last", seed=902)
+    inp = make_inputs(w)
+    inp["parent"][0, 40] = 10
+    o, st, cc, status, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
+    assert status == lbx.LBX_ETREE
+    _assert_untouched(inp, o, st, cc)

@@ -1,0 +1,583 @@
+// gdn_step.cuh -- the tree-verify step kernel (CUDA cores, fp32).
+//
+// One CTA owns one work item: (layer l, request b, value head h, block of R
+// state rows).  Rows of the d_v x d_k state evolve independently given the
+// node inputs (k, q, a, b) and their own value entry, so the item is
+// self-contained.  Per item:
+//
+//   1. the state rows S0 of slot[b] are copied asynchronously into shared
+//      memory (16-byte chunks, XOR-swizzled);
+//   2. tree tables: depth, conv windows, and for every node n the list of the
+//      nodes on its parent's root path with the decay products between them;
+//   3. prologue: conv + SiLU (+ L2 for k and q, q_scale folded into q) for
+//      every node, written to shared memory; v only for the item's rows;
+//   4. Gram entries k_j.k_n and k_j.q_n for j on the parent path of n;
+//   5. S0 [k_0..k_{N-1} q_0..q_{N-1}]: a register-tiled fp32 product;
+//   6. per row, in node order, the delta coefficients
+//        u_n   = S_p k_n = gamma_p (S0 k_n) + sum_j g(j->p) delta_j (k_j.k_n)
+//        delta_n = b_n (v_n - a_n u_n)
+//      which is the gated delta rule in its factored form
+//        S_n = a_n S_p + delta_n k_n^T,  S_n = gamma_n S0 + sum_j g(j->n) delta_j k_j^T;
+//   7. o_n = a_n (S_p q_n) + delta_n (k_n.q_n) for every node;
+//   8. epilogues: the accepted node's state rows (persist, in place), or every
+//      node's state rows (snapshots for the unfused persist).
+//
+// Ancestor states are never materialised: each node costs two dot products
+// per row against S0 plus a short sum over its path.
+//
+// Chain mode runs the same steps over consecutive chunks of a chain, keeping
+// the running state in shared memory and advancing it to the end of each
+// chunk with the same factored form.
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace lbx {
+
+struct StepArgs {
+  int L, Bq, N, Hk, Hv, K, n_slots;
+  float l2_eps, q_scale;
+  int chain;  // 0: one tree of N nodes; 1: a chain processed in chunks of `cap`
+  int cap;    // node capacity of one pass (N in tree mode)
+  const uint16_t *x;         // [L][Bq][N][C] bf16 (fused)
+  const uint16_t *conv_w;    // [L][C][K] bf16 (fused)
+  const float *conv_cache;   // [L][n_slots][K-1][C] (fused: read, and written when persisting)
+  const float *qkv;          // [L][Bq][N][C] fp32 (unfused)
+  const uint16_t *a, *b;     // [L][Bq][N][Hv] bf16
+  const int32_t *parent;     // [Bq][N]
+  const int32_t *slot;       // [Bq]
+  const int32_t *accepted;   // [Bq] (persist)
+  const float *state_in;     // [L][n_slots][Hv][d][d]
+  float *state_out;          // persist target (== state_in when fused)
+  float *conv_cache_out;     // persist target (== conv_cache when fused)
+  float *o;                  // [L][Bq][N][Hv][d]
+  float *node_states;        // [L][Bq][N][Hv][d][d] (snapshots) or NULL
+  unsigned int *counters;    // [L][Bq][Hk] arrival counters (fused persist)
+  int32_t *status;
+};
+
+// Shared-memory carve-up of one item; identical on host and device.
+struct StepLayout {
+  int s0, kq, skq, v, del, pj, pg, ckk, ckq, par, dep, off, win, an, bn, gam, kqn, crow, misc,
+      total;
+  int kq_rows, skq_ld, npair;
+};
+
+__host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
+
+__host__ __device__ inline StepLayout step_layout(int D, int R, int TC, int CG, int cap) {
+  StepLayout Ly;
+  int o = 0;
+  Ly.kq_rows = CG * TC;
+  Ly.skq_ld = R + 4;
+  Ly.npair = cap > 1 ? cap * (cap - 1) / 2 : 1;
+  Ly.s0 = o;   o = align16(o + R * D * 4);
+  Ly.kq = o;   o = align16(o + Ly.kq_rows * D * 4);
+  Ly.skq = o;  o = align16(o + 2 * cap * Ly.skq_ld * 4);
+  Ly.v = o;    o = align16(o + cap * R * 4);
+  Ly.del = o;  o = align16(o + cap * R * 4);
+  Ly.pj = o;   o = align16(o + Ly.npair * 4);
+  Ly.pg = o;   o = align16(o + Ly.npair * 4);
+  Ly.ckk = o;  o = align16(o + Ly.npair * 4);
+  Ly.ckq = o;  o = align16(o + Ly.npair * 4);
+  Ly.par = o;  o = align16(o + cap * 4);
+  Ly.dep = o;  o = align16(o + cap * 4);
+  Ly.off = o;  o = align16(o + (cap + 1) * 4);
+  Ly.win = o;  o = align16(o + cap * LBX_MAX_CONV_WIDTH * 4);
+  Ly.an = o;   o = align16(o + cap * 4);
+  Ly.bn = o;   o = align16(o + cap * 4);
+  Ly.gam = o;  o = align16(o + cap * 4);
+  Ly.kqn = o;  o = align16(o + cap * 4);
+  Ly.crow = o; o = align16(o + LBX_MAX_CONV_WIDTH * 4);
+  Ly.misc = o; o = align16(o + 8 * 4);
+  Ly.total = o;
+  return Ly;
+}
+
+// Conv + SiLU of 8 consecutive channels c0..c0+7 of one node, whose window
+// rows are win[0..KK) (>= 0: an x row of this (layer, request); < 0: cache row
+// -1-w).  Tap KK-1 multiplies the node itself.  conv_w holds each channel's KK
+// taps contiguously, so the 8 channels' taps are 8*KK consecutive bf16.
+template <int KK>
+__device__ __forceinline__ void conv8_k(float (&out)[8], const int *win, const uint16_t *x_lb,
+                                        int C, const uint16_t *w_l, const float *cache_s, int c0) {
+  float wt[8][KK];
+  if (KK == 4 || KK == 2) {
+    // 16*KK bytes from a 16-byte boundary: KK 16-byte loads
+    uint32_t w32[4 * KK];
+    const uint4 *wp = reinterpret_cast<const uint4 *>(w_l + (size_t)c0 * KK);
+#pragma unroll
+    for (int t = 0; t < KK; ++t) {
+      const uint4 u = ldg_u4(wp + t);
+      w32[4 * t + 0] = u.x, w32[4 * t + 1] = u.y, w32[4 * t + 2] = u.z, w32[4 * t + 3] = u.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int t = 0; t < KK; ++t) {
+        const int wi = e * KK + t;
+        wt[e][t] = (wi & 1) ? __uint_as_float(w32[wi >> 1] & 0xffff0000u)
+                            : __uint_as_float(w32[wi >> 1] << 16);
+      }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int t = 0; t < KK; ++t) wt[e][t] = bf2f(w_l[(size_t)(c0 + e) * KK + t]);
+  }
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < KK; ++j) {
+    const int row = win[j];
+    float xv[8];
+    if (row >= 0) {
+      unpack8(ldg_u4(x_lb + (size_t)row * C + c0), xv);
+    } else {
+      // coherent loads: the fused kernel rewrites the cache after every
+      // reader of a row has finished with it
+      const float4 *cp = reinterpret_cast<const float4 *>(cache_s + (size_t)(-1 - row) * C + c0);
+      const float4 lo = cp[0], hi = cp[1];
+      xv[0] = lo.x, xv[1] = lo.y, xv[2] = lo.z, xv[3] = lo.w;
+      xv[4] = hi.x, xv[5] = hi.y, xv[6] = hi.z, xv[7] = hi.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wt[e][KK - 1 - j], xv[e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) out[e] = silu(acc[e]);
+}
+
+__device__ __forceinline__ void conv8(float (&out)[8], const int *win, int K, const uint16_t *x_lb,
+                                      int C, const uint16_t *w_l, const float *cache_s, int c0) {
+  switch (K) {
+    case 4: conv8_k<4>(out, win, x_lb, C, w_l, cache_s, c0); break;
+    case 3: conv8_k<3>(out, win, x_lb, C, w_l, cache_s, c0); break;
+    case 2: conv8_k<2>(out, win, x_lb, C, w_l, cache_s, c0); break;
+    default: conv8_k<1>(out, win, x_lb, C, w_l, cache_s, c0); break;
+  }
+}
+
+// New conv-cache entries of one channel: row r takes crow[r] (>= 0: x row;
+// < 0: old cache row -1-crow[r]).  Reads every old value before writing.
+__device__ __forceinline__ void persist_conv_channel(int c, int K, int C, const int *crow,
+                                                     const uint16_t *x_lb, const float *cache_in,
+                                                     float *cache_out) {
+  float old[LBX_MAX_CONV_WIDTH];
+#pragma unroll
+  for (int r = 0; r < LBX_MAX_CONV_WIDTH - 1; ++r)
+    if (r < K - 1) old[r] = cache_in[(size_t)r * C + c];
+#pragma unroll
+  for (int r = 0; r < LBX_MAX_CONV_WIDTH - 1; ++r)
+    if (r < K - 1) {
+      const int w = crow[r];
+      float v = 0.f;
+      if (w >= 0) {
+        v = bf2f(x_lb[(size_t)w * C + c]);
+      } else {
+#pragma unroll
+        for (int s = 0; s < LBX_MAX_CONV_WIDTH - 1; ++s)
+          if (s == -1 - w) v = old[s];
+      }
+      cache_out[(size_t)r * C + c] = v;
+    }
+}
+
+template <int D, int R, int TC, bool FUSED, bool PERSIST, bool SNAP>
+__global__ void __launch_bounds__(kThreads) gdn_step_kernel(const StepArgs A) {
+  static_assert(D % 32 == 0 && D <= 128, "d must be 32, 64 or 128");
+  static_assert(D % R == 0 && R % 32 == 0 && R <= 128, "row block");
+  constexpr int DQ = D / 4;             // 16-byte chunks per state row
+  constexpr int RB = D / R;             // row blocks per head
+  constexpr int RG = R / 4;             // row groups of the product tile
+  constexpr int CG = kThreads / RG;     // column groups of the product tile
+  constexpr int GQ = D / 8;             // threads per (node, q|k) in the prologue
+  constexpr int GV = R / 8;             // threads per node for v
+  static_assert(kThreads % RG == 0 && CG <= 32, "tile");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StepLayout Ly = step_layout(D, R, TC, CG, A.cap);
+  float4 *S0s = reinterpret_cast<float4 *>(smem + Ly.s0);
+  float4 *KQ = reinterpret_cast<float4 *>(smem + Ly.kq);
+  float *SKQ = reinterpret_cast<float *>(smem + Ly.skq);
+  float *V = reinterpret_cast<float *>(smem + Ly.v);
+  float *DEL = reinterpret_cast<float *>(smem + Ly.del);
+  int *pj = reinterpret_cast<int *>(smem + Ly.pj);
+  float *pg = reinterpret_cast<float *>(smem + Ly.pg);
+  float *ckk = reinterpret_cast<float *>(smem + Ly.ckk);
+  float *ckq = reinterpret_cast<float *>(smem + Ly.ckq);
+  int *par = reinterpret_cast<int *>(smem + Ly.par);
+  int *dep = reinterpret_cast<int *>(smem + Ly.dep);
+  int *off = reinterpret_cast<int *>(smem + Ly.off);
+  int *win = reinterpret_cast<int *>(smem + Ly.win);
+  float *an = reinterpret_cast<float *>(smem + Ly.an);
+  float *bn = reinterpret_cast<float *>(smem + Ly.bn);
+  float *gam = reinterpret_cast<float *>(smem + Ly.gam);
+  float *kqn = reinterpret_cast<float *>(smem + Ly.kqn);
+  int *crow = reinterpret_cast<int *>(smem + Ly.crow);
+  int *misc = reinterpret_cast<int *>(smem + Ly.misc);  // [0] error flag, [1] last arriver
+  const int ldk = Ly.skq_ld;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // ---- item ----
+  int item = blockIdx.x;
+  const int rb = item % RB;
+  item /= RB;
+  const int h = item % A.Hv;
+  item /= A.Hv;
+  const int bq = item % A.Bq;
+  const int l = item / A.Bq;
+  const int N = A.N, K = A.K, Hk = A.Hk, Hv = A.Hv;
+  const int G = Hv / Hk, kh = h / G;
+  const int C = (2 * Hk + Hv) * D;
+  const size_t lb = (size_t)l * A.Bq + bq;
+
+  // ---- 1. every CTA validates the whole batch; on error nothing is written ----
+  {
+    int code = validate_batch(A.parent, A.slot, A.accepted, A.Bq, N, A.n_slots, A.chain != 0,
+                              PERSIST, PERSIST);
+    code = block_any_error(code, misc);
+    if (code) {
+      if (tid == 0 && A.status) *A.status = code;
+      return;
+    }
+  }
+  const int slot_b = A.slot[bq];
+  const size_t head_off =
+      (((size_t)l * A.n_slots + slot_b) * Hv + h) * (size_t)D * D + (size_t)rb * R * D;
+  const uint16_t *x_lb = FUSED ? A.x + lb * N * C : nullptr;
+  const uint16_t *w_l = FUSED ? A.conv_w + (size_t)l * C * K : nullptr;
+  const float *cache_s =
+      FUSED ? A.conv_cache + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C : nullptr;
+  const float *qkv_lb = FUSED ? nullptr : A.qkv + lb * N * C;
+  const uint16_t *a_lb = A.a + lb * N * Hv;
+  const uint16_t *b_lb = A.b + lb * N * Hv;
+  const int32_t *par_b = A.parent + (size_t)bq * N;
+  const int acc_b = PERSIST ? A.accepted[bq] : -1;
+
+  // ---- 2. state rows -> shared memory (async) ----
+  {
+    const float *gS = A.state_in + head_off;
+    for (int idx = tid; idx < R * DQ; idx += kThreads) {
+      const int r = idx / DQ, q = idx % DQ;
+      cp_async16(&S0s[r * DQ + swz(q, r)], gS + (size_t)r * D + q * 4);
+    }
+    cp_async_commit();
+  }
+
+  // New conv-window sources for the persist: row r of the new window is the
+  // (K-2-r)-th ancestor of the accepted node, or, where the path is too short,
+  // old cache row depth(acc)+1+r.
+  if (FUSED && PERSIST && tid == 0) {
+    int depth_acc = 0;
+    if (A.chain) depth_acc = acc_b;
+    else
+      for (int m = acc_b; m > 0; m = par_b[m]) ++depth_acc;
+    for (int r = 0; r < K - 1; ++r) {
+      const int dist = K - 2 - r;
+      int w;
+      if (dist <= depth_acc) {
+        if (A.chain) w = acc_b - dist;
+        else {
+          int m = acc_b;
+          for (int s = 0; s < dist; ++s) m = par_b[m];
+          w = m;
+        }
+      } else {
+        w = -1 - (depth_acc + 1 + r);
+      }
+      crow[r] = w;
+    }
+  }
+
+  const int n_chunks = A.chain ? (N + A.cap - 1) / A.cap : 1;
+  for (int ch = 0; ch < n_chunks; ++ch) {
+    const int t0 = ch * A.cap;
+    const int n = A.chain ? min(A.cap, N - t0) : N;
+
+    // ---- 3a. per-node tables ----
+    for (int i = tid; i < n; i += kThreads) {
+      int p, dpt;
+      if (A.chain) {
+        p = i - 1;
+        dpt = i;
+      } else {
+        p = par_b[i];
+        dpt = 0;
+        for (int m = i; m > 0; m = par_b[m]) ++dpt;
+      }
+      par[i] = p;
+      dep[i] = dpt;
+      an[i] = bf2f(a_lb[(size_t)(t0 + i) * Hv + h]);
+      bn[i] = bf2f(b_lb[(size_t)(t0 + i) * Hv + h]);
+      if (FUSED) {
+        if (A.chain) {
+          for (int j = 0; j < K; ++j) {
+            const int tt = t0 + i - j;
+            win[i * LBX_MAX_CONV_WIDTH + j] = tt >= 0 ? tt : -1 - (K - 1 + tt);
+          }
+        } else {
+          int m = i, past = 0;
+          for (int j = 0; j < K; ++j) {
+            if (m >= 0) {
+              win[i * LBX_MAX_CONV_WIDTH + j] = m;
+              m = par_b[m];
+            } else {
+              ++past;
+              win[i * LBX_MAX_CONV_WIDTH + j] = -1 - (K - 1 - past);
+            }
+          }
+        }
+      }
+    }
+    // pad columns of the product tile read zeros
+    for (int idx = 2 * n * DQ + tid; idx < Ly.kq_rows * DQ; idx += kThreads)
+      KQ[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    if (tid == 0) {
+      off[0] = 0;
+      for (int i = 0; i < n; ++i) off[i + 1] = off[i] + dep[i];
+    }
+    __syncthreads();
+
+    // ---- 3b. parent-path lists: for node i, j runs up from parent(i) to the
+    // chunk root; pg = product of the gates strictly below j on that path ----
+    for (int i = tid; i < n; i += kThreads) {
+      int j = par[i];
+      float g = 1.f;
+      for (int e = off[i]; e < off[i + 1]; ++e) {
+        pj[e] = j;
+        pg[e] = g;
+        g *= an[j];
+        j = par[j];
+      }
+      gam[i] = g;  // product of the gates over the whole parent path
+    }
+
+    // ---- 3c. prologue: k and q rows (unit norm, q scaled), v entries ----
+    {
+      const int units = 2 * n * GQ;
+      for (int base = 0; base < units; base += kThreads) {
+        const int u = base + tid;
+        const bool act = u < units;
+        const int grp = act ? u / GQ : 0, li = u % GQ;
+        const bool is_q = grp >= n;
+        const int i = is_q ? grp - n : grp;
+        const int c0 = (is_q ? 0 : Hk * D) + kh * D + li * 8;
+        float v8[8];
+        if (act) {
+          if (FUSED) {
+            conv8(v8, win + i * LBX_MAX_CONV_WIDTH, K, x_lb, C, w_l, cache_s, c0);
+          } else {
+            const float *src = qkv_lb + (size_t)(t0 + i) * C + c0;
+            float4 lo = ldg_f4(src), hi = ldg_f4(src + 4);
+            v8[0] = lo.x, v8[1] = lo.y, v8[2] = lo.z, v8[3] = lo.w;
+            v8[4] = hi.x, v8[5] = hi.y, v8[6] = hi.z, v8[7] = hi.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+        }
+        float scale = is_q ? A.q_scale : 1.f;
+        if (FUSED) {
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
+#pragma unroll
+          for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          scale *= rsqrtf(ss + A.l2_eps);
+        }
+        if (act) {
+          KQ[grp * DQ + swz(2 * li, grp)] =
+              make_float4(scale * v8[0], scale * v8[1], scale * v8[2], scale * v8[3]);
+          KQ[grp * DQ + swz(2 * li + 1, grp)] =
+              make_float4(scale * v8[4], scale * v8[5], scale * v8[6], scale * v8[7]);
+        }
+      }
+      const int vunits = n * GV;
+      for (int u = tid; u < vunits; u += kThreads) {
+        const int i = u / GV, li = u % GV;
+        const int c0 = 2 * Hk * D + h * D + rb * R + li * 8;
+        float v8[8];
+        if (FUSED) {
+          conv8(v8, win + i * LBX_MAX_CONV_WIDTH, K, x_lb, C, w_l, cache_s, c0);
+        } else {
+          const float *src = qkv_lb + (size_t)(t0 + i) * C + c0;
+          float4 lo = ldg_f4(src), hi = ldg_f4(src + 4);
+          v8[0] = lo.x, v8[1] = lo.y, v8[2] = lo.z, v8[3] = lo.w;
+          v8[4] = hi.x, v8[5] = hi.y, v8[6] = hi.z, v8[7] = hi.w;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(V + i * R + li * 8);
+        dst[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+        dst[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+      }
+    }
+    __syncthreads();
+
+    // ---- conv-cache persist (after this CTA's last read of the old cache) ----
+    if (FUSED && PERSIST && ch == 0) {
+      float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
+      // v channels of this row block: only this CTA reads them
+      for (int j = tid; j < R; j += kThreads)
+        persist_conv_channel(2 * Hk * D + h * D + rb * R + j, K, C, crow, x_lb, cache_s, cache_o);
+      // q/k channels of key head kh are read by G*RB CTAs; the last to arrive
+      // writes them, after all the others have finished reading.
+      if (tid == 0) {
+        __threadfence();
+        unsigned int *cnt = A.counters + lb * Hk + kh;
+        const unsigned int prev = atomicAdd(cnt, 1u);
+        const int last = prev == (unsigned int)(G * RB - 1);
+        if (last) {
+          atomicExch(cnt, 0u);
+          __threadfence();
+        }
+        misc[1] = last;
+      }
+      __syncthreads();
+      if (misc[1])
+        for (int j = tid; j < 2 * D; j += kThreads)
+          persist_conv_channel(j < D ? kh * D + j : Hk * D + kh * D + (j - D), K, C, crow, x_lb,
+                               cache_s, cache_o);
+    }
+
+    // ---- 4. Gram entries (warp per node) ----
+    for (int i = warp; i < n; i += kThreads / 32) {
+      const bool on = lane < DQ;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 ki = on ? KQ[i * DQ + swz(lane, i)] : z;
+      const float4 qi = on ? KQ[(n + i) * DQ + swz(lane, n + i)] : z;
+      const float kq = warp_sum(dot4(ki, qi));
+      if (lane == 0) kqn[i] = kq;
+      for (int e = off[i]; e < off[i + 1]; ++e) {
+        const int j = pj[e];
+        const float4 kj = on ? KQ[j * DQ + swz(lane, j)] : z;
+        const float s1 = warp_sum(dot4(kj, ki));
+        const float s2 = warp_sum(dot4(kj, qi));
+        if (lane == 0) {
+          ckk[e] = pg[e] * s1;
+          ckq[e] = pg[e] * s2;
+        }
+      }
+    }
+    if (ch == 0) cp_async_wait_all();
+    __syncthreads();
+
+    // ---- 5. SKQ[c][r] = S0[r] . KQ[c]  for c < 2n (k columns, then q) ----
+    {
+      const int cg = tid % CG, rg = tid / CG;
+      float acc[4][TC];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TC; ++j) acc[i][j] = 0.f;
+      for (int q0 = 0; q0 < DQ; q0 += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float4 s[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = rg + RG * i;
+            s[i] = S0s[r * DQ + (q0 | ((u ^ r) & 7))];
+          }
+#pragma unroll
+          for (int j = 0; j < TC; ++j) {
+            const int c = cg + CG * j;
+            const float4 kv = KQ[c * DQ + (q0 | ((u ^ c) & 7))];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[i][j] = fmaf(s[i].x, kv.x, acc[i][j]);
+              acc[i][j] = fmaf(s[i].y, kv.y, acc[i][j]);
+              acc[i][j] = fmaf(s[i].z, kv.z, acc[i][j]);
+              acc[i][j] = fmaf(s[i].w, kv.w, acc[i][j]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < TC; ++j) {
+        const int c = cg + CG * j;
+        if (c < 2 * n)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) SKQ[c * ldk + rg + RG * i] = acc[i][j];
+      }
+    }
+    __syncthreads();
+
+    // ---- 6. delta_n per row, nodes in topological order ----
+    if (tid < R) {
+      const int r = tid;
+      for (int i = 0; i < n; ++i) {
+        float u = gam[i] * SKQ[i * ldk + r];
+        for (int e = off[i]; e < off[i + 1]; ++e) u = fmaf(ckk[e], DEL[pj[e] * R + r], u);
+        DEL[i * R + r] = bn[i] * (V[i * R + r] - an[i] * u);
+      }
+    }
+    __syncthreads();
+
+    // ---- 7. o_n = a_n (S_p q_n) + delta_n (k_n . q_n) ----
+    {
+      constexpr int R4 = R / 4;
+      const float4 *SKQ4 = reinterpret_cast<const float4 *>(SKQ);
+      const float4 *DEL4 = reinterpret_cast<const float4 *>(DEL);
+      for (int idx = tid; idx < n * R4; idx += kThreads) {
+        const int i = idx / R4, r4 = idx % R4;
+        float4 acc = f4_scale(gam[i], SKQ4[(n + i) * (ldk / 4) + r4]);
+        for (int e = off[i]; e < off[i + 1]; ++e) {
+          const float4 dj = DEL4[pj[e] * R4 + r4];
+          const float c = ckq[e];
+          acc.x = fmaf(c, dj.x, acc.x);
+          acc.y = fmaf(c, dj.y, acc.y);
+          acc.z = fmaf(c, dj.z, acc.z);
+          acc.w = fmaf(c, dj.w, acc.w);
+        }
+        const float4 di = DEL4[i * R4 + r4];
+        const float ai = an[i], kq = kqn[i];
+        float4 out;
+        out.x = fmaf(ai, acc.x, kq * di.x);
+        out.y = fmaf(ai, acc.y, kq * di.y);
+        out.z = fmaf(ai, acc.z, kq * di.z);
+        out.w = fmaf(ai, acc.w, kq * di.w);
+        stg_f4(A.o + (((lb * N + t0 + i) * Hv + h) * (size_t)D + rb * R + 4 * r4), out);
+      }
+    }
+
+    // ---- 8. state epilogues: S_t rows = gamma_t S0 + sum_{j on path(t)} g(j->t) delta_j k_j^T
+    // Target path of node t: t itself with coefficient 1, then its parent-path
+    // list with coefficients pg * a_t; gamma_t = gam[t] * a_t.
+    auto state_rows = [&](int t, float *dst_base, bool to_smem) {
+      const float gt = gam[t] * an[t];
+      const float at = an[t];
+      for (int idx = tid; idx < R * DQ; idx += kThreads) {
+        const int r = idx / DQ, q = idx % DQ;
+        const int sidx = r * DQ + swz(q, r);
+        float4 acc = f4_scale(gt, S0s[sidx]);
+        f4_fma(acc, DEL[t * R + r], KQ[t * DQ + swz(q, t)]);
+        for (int e = off[t]; e < off[t + 1]; ++e) {
+          const int j = pj[e];
+          f4_fma(acc, pg[e] * at * DEL[j * R + r], KQ[j * DQ + swz(q, j)]);
+        }
+        if (to_smem) S0s[sidx] = acc;
+        else stg_f4(dst_base + (size_t)r * D + 4 * q, acc);
+      }
+    };
+    if (PERSIST) {
+      const int ia = acc_b - t0;
+      if (ia >= 0 && ia < n) state_rows(ia, A.state_out + head_off, false);
+    }
+    if (SNAP) {
+      for (int t = 0; t < n; ++t)
+        state_rows(t, A.node_states + (((lb * N + t0 + t) * Hv + h) * (size_t)D * D) + (size_t)rb * R * D,
+                   false);
+    }
+    if (A.chain && ch + 1 < n_chunks) {
+      // advance the running state to the end of this chunk (each element is
+      // read and rewritten by the thread that owns it)
+      state_rows(n - 1, nullptr, true);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace lbx

@@ -1,0 +1,169 @@
+"""Thin Python binding of the liblbx C ABI (include/lbx.h).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of liblbx.so.  The functions keep the C names and argument order and
+take torch CUDA tensors (PyTorch supplies device memory and streams).  bf16
+arguments may be ``torch.bfloat16`` or 16-bit integer tensors holding bf16 bit
+patterns.  There is no CPU fallback: if the library cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblbx.so")
+
+LBX_OK, LBX_EINVAL, LBX_ECUDA, LBX_ETREE = 0, -1, -2, -3
+LBX_MAX_TREE_NODES = 64
+LBX_CHAIN_CHUNK = 64
+LBX_MAX_CONV_WIDTH = 4
+LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED = 0, 1, 2
+
+# Every function the header declares, in header order.
+EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
+           "lbx_tree_persist", "lbx_verify_step")
+
+
+class LbxError(RuntimeError):
+    def __init__(self, fn: str, rc: int):
+        super().__init__(f"{fn} failed: {rc} ({strerror(rc)})")
+        self.rc = rc
+
+
+class lbx_cfg(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int), ("Bq", ctypes.c_int), ("N", ctypes.c_int),
+                ("Hk", ctypes.c_int), ("Hv", ctypes.c_int), ("d", ctypes.c_int),
+                ("K", ctypes.c_int), ("n_slots", ctypes.c_int), ("l2_eps", ctypes.c_float),
+                ("q_scale", ctypes.c_float), ("mode", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblbx.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"liblbx.so not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        lib.lbx_strerror.restype = ctypes.c_char_p
+        lib.lbx_strerror.argtypes = [i32]
+        lib.lbx_workspace_size.restype = ctypes.c_size_t
+        lib.lbx_workspace_size.argtypes = [vp]
+        lib.lbx_tree_conv.restype = i32
+        lib.lbx_tree_conv.argtypes = [vp] * 9
+        lib.lbx_tree_deltanet.restype = i32
+        lib.lbx_tree_deltanet.argtypes = [vp] * 11
+        lib.lbx_tree_persist.restype = i32
+        lib.lbx_tree_persist.argtypes = [vp] * 11
+        lib.lbx_verify_step.restype = i32
+        lib.lbx_verify_step.argtypes = [vp] * 11 + [vp, ctypes.c_size_t, vp, vp]
+        _lib = lib
+    return _lib
+
+
+def strerror(rc: int) -> str:
+    return load().lbx_strerror(rc).decode()
+
+
+def make_cfg(L, Bq, N, Hk, Hv, d, K=4, n_slots=None, l2_eps=1e-6, q_scale=1.0,
+             mode=LBX_MODE_AUTO) -> lbx_cfg:
+    return lbx_cfg(L=L, Bq=Bq, N=N, Hk=Hk, Hv=Hv, d=d, K=K,
+                   n_slots=Bq if n_slots is None else n_slots, l2_eps=l2_eps, q_scale=q_scale,
+                   mode=mode)
+
+
+def cfg_of(w, mode=LBX_MODE_AUTO) -> lbx_cfg:
+    """Config from an inputs.Workload."""
+    return make_cfg(w.L, w.Bq, w.N, w.Hk, w.Hv, w.d, w.K, w.n_slots, w.l2_eps, w.q_scale, mode)
+
+
+_BF16_OK = (torch.bfloat16, torch.int16, getattr(torch, "uint16", torch.int16))
+
+
+def _ptr(t: Optional[torch.Tensor], dtypes=None, name="") -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    return t.data_ptr()
+
+
+def _bf(t, name):
+    return _ptr(t, _BF16_OK, name)
+
+
+def _f32(t, name):
+    return _ptr(t, (torch.float32,), name)
+
+
+def _i32(t, name):
+    return _ptr(t, (torch.int32,), name)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != LBX_OK:
+        raise LbxError(fn, rc)
+
+
+def lbx_workspace_size(cfg: lbx_cfg) -> int:
+    return int(load().lbx_workspace_size(ctypes.byref(cfg)))
+
+
+def lbx_tree_conv(cfg, x, conv_w, conv_cache, parent, slot, qkv_out, d_status=None, stream=None):
+    _check("lbx_tree_conv", load().lbx_tree_conv(
+        ctypes.byref(cfg), _bf(x, "x"), _bf(conv_w, "conv_w"), _f32(conv_cache, "conv_cache"),
+        _i32(parent, "parent"), _i32(slot, "slot"), _f32(qkv_out, "qkv_out"),
+        _i32(d_status, "d_status"), _stream(stream)))
+
+
+def lbx_tree_deltanet(cfg, qkv, a, b, state, parent, slot, o, node_states=None, d_status=None,
+                      stream=None):
+    _check("lbx_tree_deltanet", load().lbx_tree_deltanet(
+        ctypes.byref(cfg), _f32(qkv, "qkv"), _bf(a, "a"), _bf(b, "b"), _f32(state, "state"),
+        _i32(parent, "parent"), _i32(slot, "slot"), _f32(o, "o"),
+        _f32(node_states, "node_states"), _i32(d_status, "d_status"), _stream(stream)))
+
+
+def lbx_tree_persist(cfg, x, node_states, parent, slot, accepted, state, conv_cache,
+                     d_status=None, stream=None):
+    _check("lbx_tree_persist", load().lbx_tree_persist(
+        ctypes.byref(cfg), _bf(x, "x"), _f32(node_states, "node_states"), _i32(parent, "parent"),
+        _i32(slot, "slot"), _i32(accepted, "accepted"), _f32(state, "state"),
+        _f32(conv_cache, "conv_cache"), _i32(d_status, "d_status"), _stream(stream)))
+
+
+def lbx_verify_step(cfg, x, conv_w, a, b, parent, slot, accepted, state, conv_cache, o,
+                    workspace, d_status=None, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("lbx_verify_step", load().lbx_verify_step(
+        ctypes.byref(cfg), _bf(x, "x"), _bf(conv_w, "conv_w"), _bf(a, "a"), _bf(b, "b"),
+        _i32(parent, "parent"), _i32(slot, "slot"), _i32(accepted, "accepted"),
+        _f32(state, "state"), _f32(conv_cache, "conv_cache"), _f32(o, "o"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _i32(d_status, "d_status"),
+        _stream(stream)))
+
+
+def new_workspace(cfg: lbx_cfg, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of lbx_workspace_size(cfg) bytes."""
+    n = lbx_workspace_size(cfg)
+    if n == 0:
+        raise LbxError("lbx_workspace_size", LBX_EINVAL)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
