@@ -165,6 +165,36 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
                     float *o, void *workspace, size_t workspace_bytes, int32_t *d_status,
                     cudaStream_t stream);
 
+/* Capacity of lbx_verify_step_noalloc: L * Bq * Hk <= LBX_NOALLOC_MAX_GROUPS. */
+#define LBX_NOALLOC_MAX_GROUPS 65536
+
+/*
+ * lbx_verify_step without a workspace, for callers that cannot allocate
+ * device memory -- for instance an engine that reserves all device memory
+ * for its caches up front and allows no later cudaMalloc (which would also
+ * synchronise the device), or a plugin inside a host framework that owns the
+ * only allocator.  The paper has no counterpart to this entry point.
+ *
+ * Arguments and results are those of lbx_verify_step minus the workspace.
+ * The arrival counters live in a fixed device array inside the library
+ * (LBX_NOALLOC_MAX_GROUPS counters, 256 KB), which every GPU that loads the
+ * library keeps until the process exits.  Configurations with
+ * L * Bq * Hk > LBX_NOALLOC_MAX_GROUPS are rejected with LBX_EINVAL.
+ * The function allocates nothing: no cudaMalloc, cudaFree or other
+ * allocating call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call clears the counters it uses (cudaMemsetAsync on `stream`)
+ *     before launching, since the array keeps the previous call's contents.
+ *   - All calls on a device share the one array: calls that overlap on the
+ *     GPU (other streams, other host threads) race on it.  Serialise them.
+ */
+int lbx_verify_step_noalloc(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_w,
+                            const uint16_t *a, const uint16_t *b, const int32_t *parent,
+                            const int32_t *slot, const int32_t *accepted, float *state,
+                            float *conv_cache, float *o, int32_t *d_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED = 0, 1, 2
 
 # Every function the header declares, in header order.
 EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
-           "lbx_tree_persist", "lbx_verify_step")
+           "lbx_tree_persist", "lbx_verify_step", "lbx_verify_step_noalloc")
+LBX_NOALLOC_MAX_GROUPS = 65536
 
 
 class LbxError(RuntimeError):
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lbx_tree_persist.argtypes = [vp] * 11
         lib.lbx_verify_step.restype = i32
         lib.lbx_verify_step.argtypes = [vp] * 11 + [vp, ctypes.c_size_t, vp, vp]
+        lib.lbx_verify_step_noalloc.restype = i32
+        lib.lbx_verify_step_noalloc.argtypes = [vp] * 13
         _lib = lib
     return _lib
 
@@ -159,6 +162,17 @@ def lbx_verify_step(cfg, x, conv_w, a, b, parent, slot, accepted, state, conv_ca
         _f32(state, "state"), _f32(conv_cache, "conv_cache"), _f32(o, "o"),
         _ptr(workspace, None, "workspace"), ws_bytes, _i32(d_status, "d_status"),
         _stream(stream)))
+
+
+def lbx_verify_step_noalloc(cfg, x, conv_w, a, b, parent, slot, accepted, state, conv_cache, o,
+                            d_status=None, stream=None):
+    """lbx_verify_step for callers that cannot allocate: the arrival counters
+    live in a fixed array inside the library (see include/lbx.h)."""
+    _check("lbx_verify_step_noalloc", load().lbx_verify_step_noalloc(
+        ctypes.byref(cfg), _bf(x, "x"), _bf(conv_w, "conv_w"), _bf(a, "a"), _bf(b, "b"),
+        _i32(parent, "parent"), _i32(slot, "slot"), _i32(accepted, "accepted"),
+        _f32(state, "state"), _f32(conv_cache, "conv_cache"), _f32(o, "o"),
+        _i32(d_status, "d_status"), _stream(stream)))
 
 
 def new_workspace(cfg: lbx_cfg, device="cuda") -> torch.Tensor:
