@@ -59,6 +59,7 @@ extern "C" {
 #define LBX_EINVAL (-1) /* bad dimension, NULL pointer, size over a limit   */
 #define LBX_ECUDA (-2)  /* a CUDA call or kernel launch failed               */
 #define LBX_ETREE (-3)  /* invalid tree (device-detected, via d_status)      */
+#define LBX_ETIMEOUT (-4) /* a bounded in-kernel wait gave up (via d_status) */
 
 /* Limits. */
 #define LBX_MAX_TREE_NODES 64 /* tree mode: N <= 64 nodes per request          */
@@ -69,6 +70,8 @@ extern "C" {
 #define LBX_MODE_AUTO 0    /* tree if N <= LBX_MAX_TREE_NODES, else chunked     */
 #define LBX_MODE_TREE 1    /* arbitrary tree, N <= LBX_MAX_TREE_NODES           */
 #define LBX_MODE_CHUNKED 2 /* chain only (parent[i] == i-1), any N >= 1         */
+#define LBX_MODE_TREE_CUDA_CORES 3 /* tree mode forced onto the CUDA-core kernel
+                                      (same results; for cross-checking)       */
 
 typedef struct lbx_cfg {
   int L;       /* gated-DeltaNet layers in the call (>= 1)                     */

@@ -228,3 +228,56 @@ def test_chunked_mode_rejects_a_non_chain():
     o, st, cc, status, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
     assert status == lbx.LBX_ETREE
     _assert_untouched(inp, o, st, cc)
+
+
+# -------------------------------------------------------------------------
+# Tensor-core kernel (d = 128, tree mode, N <= 24): shapes at its limits,
+# and agreement with the CUDA-core kernel on the same inputs.
+# -------------------------------------------------------------------------
+def tc(**kw):
+    base = dict(name="tc", L=2, Bq=2, N=22, Hk=2, Hv=6, d=128, tree="ddtree", accepted="node",
+                seed=1100)
+    base.update(kw)
+    return Workload(**base)
+
+
+TC_EDGE = {
+    "n1": tc(N=1, seed=1101),
+    "n2": tc(N=2, seed=1102),
+    "n8": tc(N=8, seed=1103),
+    "n9": tc(N=9, seed=1104),
+    "n16": tc(N=16, tree="uniform", seed=1105),
+    "n24_chain": tc(N=24, tree="chain", accepted="last", seed=1106),
+    "n24_uniform": tc(N=24, tree="uniform", seed=1107),
+    "g1": tc(Hk=3, Hv=3, seed=1108),
+    "g4": tc(Hk=1, Hv=4, seed=1109),
+    "three_requests": tc(Bq=3, N=13, seed=1110),
+    "k2": tc(K=2, seed=1111),
+    "k1": tc(K=1, seed=1112),
+    "q_scale": tc(q_scale=float(1 / np.sqrt(128)), seed=1113),
+    "leaf": tc(accepted="leaf", seed=1114),
+    "many_tiles": tc(L=7, Bq=3, Hk=4, Hv=12, N=22, seed=1115),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TC_EDGE))
+def test_tensor_core_edge_cases(name):
+    w = TC_EDGE[name]
+    slots = np.array([3, 0, 4], dtype=np.int32) if w.Bq == 3 else None
+    inp = make_inputs(w, slots=slots)
+    o, st, cc, status, ws = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
+    assert status == 0
+    check_verify(w, inp, o, st, cc)
+    assert not ws.any()
+
+
+def test_tensor_core_and_cuda_core_kernels_agree_full_step():
+    w = WORKLOADS["step27b"]
+    inp = make_inputs(w)
+    o1, s1, c1, st1, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
+    o2, s2, c2, st2, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE_CUDA_CORES)
+    assert st1 == st2 == 0
+    assert np.abs(o1 - o2).max() <= 1e-4 * np.abs(o2).max()
+    assert c1.tobytes() == c2.tobytes()
+    rel = np.linalg.norm((s1 - s2)[:, :1].reshape(-1)) / np.linalg.norm(s2[:, :1].reshape(-1))
+    assert rel <= 1e-5

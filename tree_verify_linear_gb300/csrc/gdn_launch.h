@@ -37,6 +37,10 @@ int launch_step_fused(const StepArgs &A, int d, cudaStream_t st);
 // Recurrence from a conv output; node_states written when A.node_states != NULL.
 int launch_step_unfused(const StepArgs &A, int d, cudaStream_t st);
 
+// Tensor-core fused step (d = 128, tree mode, N <= 24).
+bool step_tc_supported(int d, int N, int chain);
+int launch_step_tc(const StepArgs &A, cudaStream_t st);
+
 // Row-block size and product-tile width used for head dimension d and node
 // capacity cap; returns the dynamic shared memory bytes (0 if unsupported).
 int step_smem_bytes(int d, int cap);

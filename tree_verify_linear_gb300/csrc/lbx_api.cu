@@ -53,6 +53,7 @@ const char *lbx_strerror(int status) {
     case LBX_EINVAL: return "invalid argument (dimension, pointer, alignment, limit or index)";
     case LBX_ECUDA: return "CUDA launch or runtime error";
     case LBX_ETREE: return "invalid draft tree (parent array is not a topologically numbered tree, or not a chain in chunked mode)";
+    case LBX_ETIMEOUT: return "a bounded wait inside a kernel gave up (reported through d_status)";
   }
   return "unknown status";
 }
@@ -125,8 +126,9 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
   if (rc) return rc;
   int mode = cfg->mode;
   if (mode == LBX_MODE_AUTO) mode = cfg->N <= LBX_MAX_TREE_NODES ? LBX_MODE_TREE : LBX_MODE_CHUNKED;
-  if (mode != LBX_MODE_TREE && mode != LBX_MODE_CHUNKED) return LBX_EINVAL;
-  if (mode == LBX_MODE_TREE && cfg->N > LBX_MAX_TREE_NODES) return LBX_EINVAL;
+  if (mode != LBX_MODE_TREE && mode != LBX_MODE_CHUNKED && mode != LBX_MODE_TREE_CUDA_CORES)
+    return LBX_EINVAL;
+  if (mode != LBX_MODE_CHUNKED && cfg->N > LBX_MAX_TREE_NODES) return LBX_EINVAL;
   if (!ok16(x) || !ok16(conv_w) || !ok2(a) || !ok2(b) || !ok4(parent) || !ok4(slot) ||
       !ok4(accepted) || !ok16(state) || !cache_ok(cfg, conv_cache, 16) || !ok16(o) || !ok4(workspace) ||
       (d_status && !aligned(d_status, 4)))
@@ -139,6 +141,8 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
   A.parent = parent, A.slot = slot, A.accepted = accepted;
   A.state_in = state, A.state_out = state, A.conv_cache_out = conv_cache;
   A.o = o, A.counters = static_cast<unsigned int *>(workspace), A.status = d_status;
+  if (mode == LBX_MODE_TREE && lbx::step_tc_supported(cfg->d, cfg->N, A.chain))
+    return lbx::launch_step_tc(A, stream);
   return lbx::launch_step_fused(A, cfg->d, stream);
 }
 

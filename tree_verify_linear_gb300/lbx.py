@@ -18,11 +18,11 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblbx.so")
 
-LBX_OK, LBX_EINVAL, LBX_ECUDA, LBX_ETREE = 0, -1, -2, -3
+LBX_OK, LBX_EINVAL, LBX_ECUDA, LBX_ETREE, LBX_ETIMEOUT = 0, -1, -2, -3, -4
 LBX_MAX_TREE_NODES = 64
 LBX_CHAIN_CHUNK = 64
 LBX_MAX_CONV_WIDTH = 4
-LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED = 0, 1, 2
+LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED, LBX_MODE_TREE_CUDA_CORES = 0, 1, 2, 3
 
 # Every function the header declares, in header order.
 EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
