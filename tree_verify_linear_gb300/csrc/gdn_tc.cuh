@@ -49,19 +49,22 @@ struct TcLayout {
   static constexpr int NC = 2 * NMAX;
   static constexpr int kB = NC * kTcD * 4;          // one of B hi / B lo
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
+  static constexpr int TP = (NMAX + 3) & ~3;        // row pitch of T and W
   static constexpr int stage0 = 0;
   static constexpr int stage1 = stage0 + (int)kStageBytes;
   static constexpr int bhi = stage1 + (int)kStageBytes;
   static constexpr int blo = bhi + kB;
-  static constexpr int v = blo + kB;                  // [NMAX][128] fp32
-  static constexpr int del = v + NMAX * kTcD * 4;     // [NMAX][128] fp32
-  static constexpr int pj = del + NMAX * kTcD * 4;    // int   [kNPair]
-  static constexpr int gkk = pj + 4 * kNPair;         // float [kNPair]
-  static constexpr int gkq = gkk + 4 * kNPair;
-  static constexpr int ckk = gkq + 4 * kNPair;
-  static constexpr int ckq = ckk + 4 * kNPair;
-  static constexpr int tg_ = ckq + 4 * kNPair;        // float [NMAX] target coefficients
-  static constexpr int tj = tg_ + 4 * NMAX;           // int   [NMAX] target nodes
+  static constexpr int v = blo + kB;                  // [NMAX][128] fp32 v_n of the tile's head
+  static constexpr int del = v + NMAX * kTcD * 4;     // [NMAX][128] fp32 delta_n
+  static constexpr int tm = del + NMAX * kTcD * 4;    // [NMAX][TP] T = (I + diag(b a) M)^-1
+  static constexpr int wm = tm + NMAX * TP * 4;       // [NMAX][TP] W = Q T
+  static constexpr int pj = wm + NMAX * TP * 4;       // int   [kNPair] parent-path nodes
+  static constexpr int gkk = pj + 4 * kNPair;         // float [kNPair] k_j . k_n
+  static constexpr int gkq = gkk + 4 * kNPair;        // float [kNPair] k_j . q_n
+  static constexpr int ckk = gkq + 4 * kNPair;        // float [kNPair] g(j->p) k_j . k_n (per tile)
+  static constexpr int ckq = ckk + 4 * kNPair;        // float [kNPair] g(j->p) k_j . q_n (per tile)
+  static constexpr int tg_ = ckq + 4 * kNPair;        // float [NMAX] accepted-path coefficients
+  static constexpr int tj = tg_ + 4 * NMAX;           // int   [NMAX] accepted-path nodes
   static constexpr int par = tj + 4 * NMAX;
   static constexpr int dep = par + 4 * NMAX;
   static constexpr int off = dep + 4 * NMAX;          // [NMAX + 1]
@@ -70,8 +73,9 @@ struct TcLayout {
   static constexpr int bn = an + 4 * NMAX;
   static constexpr int gam = bn + 4 * NMAX;
   static constexpr int kqn = gam + 4 * NMAX;
-  static constexpr int crow = kqn + 4 * NMAX;         // [4]
-  static constexpr int misc = crow + 16;              // ints: see kernel
+  static constexpr int crow = kqn + 4 * NMAX;         // [4] conv-window sources (row threads)
+  static constexpr int ccrow = crow + 16;             // [4] same, control warp's copy
+  static constexpr int misc = ccrow + 16;             // ints: see kernel
   static constexpr int bars = (misc + 64 + 7) & ~7;   // 3 x uint64
   static constexpr int total = bars + 3 * 8;
   static_assert(kB % 1024 == 0, "operand B must keep 1024-byte alignment");
@@ -90,11 +94,56 @@ __device__ __forceinline__ uint32_t sw128_off(int rows, int row, int k) {
   return (uint32_t)(atom * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + ((k & 3) << 2));
 }
 
+// Conv-window sources of the persist: new row rr takes the (K-2-rr)-th
+// ancestor of acc, or old cache row depth(acc)+1+rr where the path is short.
+__device__ __forceinline__ void window_sources(int *dst, int K, int acc, const int32_t *par_b) {
+  int da = 0;
+  for (int m = acc; m > 0; m = par_b[m]) ++da;
+  for (int rr = 0; rr < K - 1; ++rr) {
+    const int dist = K - 2 - rr;
+    int w;
+    if (dist <= da) {
+      int m = acc;
+      for (int q = 0; q < dist; ++q) m = par_b[m];
+      w = m;
+    } else {
+      w = -1 - (da + 1 + rr);
+    }
+    dst[rr] = w;
+  }
+}
+
+// Conv-window persist of NCH channels (chan[i]) by one thread: every old
+// entry and new x value is loaded before anything is written, so the loads
+// of all channels overlap.  src[rr] >= 0: x row; < 0: old cache row -1-src.
+template <int NCH>
+__device__ __forceinline__ void persist_conv_batch(const int (&chan)[NCH], int K, int C,
+                                                   const int (&src)[LBX_MAX_CONV_WIDTH - 1],
+                                                   const uint16_t *x_lb, const float *cache_in,
+                                                   float *cache_out) {
+  float val[NCH][LBX_MAX_CONV_WIDTH - 1];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i)
+#pragma unroll
+    for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+      if (rr < K - 1) {
+        const int w = src[rr];
+        val[i][rr] = w >= 0 ? bf2f(x_lb[(size_t)w * C + chan[i]])
+                            : cache_in[(size_t)(-1 - w) * C + chan[i]];
+      }
+#pragma unroll
+  for (int i = 0; i < NCH; ++i)
+#pragma unroll
+    for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+      if (rr < K - 1) cache_out[(size_t)rr * C + chan[i]] = val[i][rr];
+}
+
 template <int NMAX>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_state, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   constexpr int NC = Ly::NC;
+  constexpr int TP = Ly::TP;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *stage[2] = {smem + Ly::stage0, smem + Ly::stage1};
@@ -102,6 +151,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char *Blo = smem + Ly::blo;
   float *V = reinterpret_cast<float *>(smem + Ly::v);
   float *DEL = reinterpret_cast<float *>(smem + Ly::del);
+  float *Tm = reinterpret_cast<float *>(smem + Ly::tm);
+  float *Wm = reinterpret_cast<float *>(smem + Ly::wm);
   int *pj = reinterpret_cast<int *>(smem + Ly::pj);
   float *gkk = reinterpret_cast<float *>(smem + Ly::gkk);
   float *gkq = reinterpret_cast<float *>(smem + Ly::gkq);
@@ -118,8 +169,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float *gam = reinterpret_cast<float *>(smem + Ly::gam);
   float *kqn = reinterpret_cast<float *>(smem + Ly::kqn);
   int *crow = reinterpret_cast<int *>(smem + Ly::crow);
+  int *ccrow = reinterpret_cast<int *>(smem + Ly::ccrow);
   int *misc = reinterpret_cast<int *>(smem + Ly::misc);
-  // misc[0] error flag, [1] abort, [2] last arriver, [3] TMEM base, [4] ntgt
+  // misc[0] error flag, [1] abort, [3] TMEM base, [4] accepted-path length
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);  // [2]
   uint64_t *mma_bar = full_bar + 2;
 
@@ -165,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[3]);
 
-  // tile -> (l, b, kh, hg) and the state row of its slab
+  // tile -> state row of its slab
   auto tile_row = [&](int t) -> int {
     const int hg = t % G, rest = t / G;
     const int kh = rest % Hk, lb = rest / Hk;
@@ -176,7 +228,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // control thread: prefetch the first tile
   const bool ctrl_lane = is_ctrl && lane == 0;
-  int pending = -1;         // stage with an issued, not yet consumed load (control thread)
+  int pending = -1;          // stage with an issued, not yet consumed load (control thread)
   uint32_t pending_par = 0;  // its phase parity
   if (ctrl_lane && count > 0) {
     const int row = tile_row(t_begin);
@@ -192,6 +244,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int hf = (warp >> 2) & 1;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quadrant
 
+  // gates of the next tile, prefetched by threads tid < N
+  float ga = 0.f, gb = 0.f;
+  if (!is_ctrl && tid < N && count > 0) {
+    const int t = t_begin, hg = t % G, rest = t / G, kh = rest % Hk, lbi = rest / Hk;
+    ga = bf2f(A.a[((size_t)lbi * N + tid) * Hv + kh * G + hg]);
+    gb = bf2f(A.b[((size_t)lbi * N + tid) * Hv + kh * G + hg]);
+  }
+
+  // control warp: the previous tile's value-head window persist is deferred
+  // until the next tile's MMAs are running
+  const uint16_t *pv_x = nullptr;
+  const float *pv_in = nullptr;
+  float *pv_out = nullptr;
+  int pv_c0 = 0;
+  int pv_src[LBX_MAX_CONV_WIDTH - 1] = {0, 0, 0};
+
   int cur_group = -1;
   for (int it = 0; it < count; ++it) {
     const int t = t_begin + it;
@@ -205,6 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint16_t *x_lb = A.x + lb * N * C;
     const uint16_t *w_l = A.conv_w + (size_t)l * C * K;
     const float *cache_s = A.conv_cache + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
+    float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
     const int32_t *par_b = A.parent + (size_t)bq * N;
     const int acc = A.accepted[bq];
     unsigned char *st = stage[s];
@@ -214,10 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (rest != cur_group) {
         cur_group = rest;
         for (int i = tid; i < N; i += kTcRowThreads) {
-          const int p = par_b[i];
           int dpt = 0;
           for (int m = i; m > 0; m = par_b[m]) ++dpt;
-          par[i] = p;
+          par[i] = par_b[i];
           dep[i] = dpt;
           int m = i, past = 0;
           for (int j = 0; j < K; ++j) {
@@ -230,24 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        if (tid == 0) {
-          // new conv-window sources: row rr <- (K-2-rr)-th ancestor of acc,
-          // or old cache row depth(acc)+1+rr when the path is too short
-          int da = 0;
-          for (int m = acc; m > 0; m = par_b[m]) ++da;
-          for (int rr = 0; rr < K - 1; ++rr) {
-            const int dist = K - 2 - rr;
-            int w;
-            if (dist <= da) {
-              int m = acc;
-              for (int q = 0; q < dist; ++q) m = par_b[m];
-              w = m;
-            } else {
-              w = -1 - (da + 1 + rr);
-            }
-            crow[rr] = w;
-          }
-        }
+        if (tid == 32) window_sources(crow, K, acc, par_b);
         ptx::named_sync(1, kTcRowThreads);
         if (tid == 0) {
           off[0] = 0;
@@ -261,31 +312,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             j = par[j];
           }
         }
-        // q/k conv + SiLU + L2 -> operand B rows (hi / lo parts); q scaled
+        // q/k conv + SiLU + L2 -> operand B rows (hi / lo parts); q scaled.
+        // All of a thread's units are loaded before any is reduced.
         {
           constexpr int GQ = kTcD / 8;  // 16 threads per (node, q|k)
+          constexpr int U = (2 * NMAX * GQ + kTcRowThreads - 1) / kTcRowThreads;
           const int units = 2 * N * GQ;
-          for (int base = 0; base < units; base += kTcRowThreads) {
-            const int u = base + tid;
-            const bool act = u < units;
-            const int grp = act ? u / GQ : 0, li = u % GQ;
+          float v8[U][8], ss[U];
+#pragma unroll
+          for (int p = 0; p < U; ++p) {
+            const int u = p * kTcRowThreads + tid;
+            const int grp = u / GQ, li = u % GQ;
             const bool is_q = grp >= N;
             const int i = is_q ? grp - N : grp;
-            const int c0 = (is_q ? 0 : Hk * kTcD) + kh * kTcD + li * 8;
-            float v8[8];
-            if (act) {
-              conv8(v8, win + i * 4, K, x_lb, C, w_l, cache_s, c0);
+            if (u < units) {
+              conv8(v8[p], win + i * 4, K, x_lb, C, w_l, cache_s,
+                    (is_q ? 0 : Hk * kTcD) + kh * kTcD + li * 8);
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+              for (int e = 0; e < 8; ++e) v8[p][e] = 0.f;
             }
-            float ss = 0.f;
+            ss[p] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
+            for (int e = 0; e < 8; ++e) ss[p] = fmaf(v8[p][e], v8[p][e], ss[p]);
+          }
 #pragma unroll
-            for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float scale = rsqrtf(ss + A.l2_eps) * (is_q ? A.q_scale : 1.f);
-            if (act) {
+          for (int p = 0; p < U; ++p)
+#pragma unroll
+            for (int o = GQ / 2; o > 0; o >>= 1) ss[p] += __shfl_xor_sync(0xffffffffu, ss[p], o);
+#pragma unroll
+          for (int p = 0; p < U; ++p) {
+            const int u = p * kTcRowThreads + tid;
+            if (u < units) {
+              const int grp = u / GQ, li = u % GQ;
+              const bool is_q = grp >= N;
+              const int i = is_q ? grp - N : grp;
+              const float scale = rsqrtf(ss[p] + A.l2_eps) * (is_q ? A.q_scale : 1.f);
               const int brow = is_q ? NMAX + i : i;
 #pragma unroll
               for (int hq = 0; hq < 2; ++hq) {
@@ -293,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float *ph = &hi.x, *pl = &lo.x;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float v = scale * v8[4 * hq + e];
+                  const float v = scale * v8[p][4 * hq + e];
                   const float vh = __uint_as_float(__float_as_uint(v) & 0xffffe000u);
                   ph[e] = vh;
                   pl[e] = v - vh;
@@ -316,28 +378,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         ptx::fence_proxy_async();
         ptx::named_sync(1, kTcRowThreads);
-        // Gram entries (warp per node): k_j.k_i and k_j.q_i for j on the
-        // parent path of i, and k_i.q_i
-        for (int i = warp; i < N; i += kTcRowThreads / 32) {
-          const uint32_t oki = sw128_off(NC, i, 4 * lane), oqi = sw128_off(NC, NMAX + i, 4 * lane);
-          float4 ki = *reinterpret_cast<const float4 *>(Bhi + oki);
-          float4 t4 = *reinterpret_cast<const float4 *>(Blo + oki);
-          ki.x += t4.x, ki.y += t4.y, ki.z += t4.z, ki.w += t4.w;
-          float4 qi = *reinterpret_cast<const float4 *>(Bhi + oqi);
-          t4 = *reinterpret_cast<const float4 *>(Blo + oqi);
-          qi.x += t4.x, qi.y += t4.y, qi.z += t4.z, qi.w += t4.w;
-          const float kq = warp_sum(dot4(ki, qi));
-          if (lane == 0) kqn[i] = kq;
-          for (int e = off[i]; e < off[i + 1]; ++e) {
-            const uint32_t okj = sw128_off(NC, pj[e], 4 * lane);
-            float4 kj = *reinterpret_cast<const float4 *>(Bhi + okj);
-            t4 = *reinterpret_cast<const float4 *>(Blo + okj);
-            kj.x += t4.x, kj.y += t4.y, kj.z += t4.z, kj.w += t4.w;
-            const float s1 = warp_sum(dot4(kj, ki));
-            const float s2 = warp_sum(dot4(kj, qi));
-            if (lane == 0) {
-              gkk[e] = s1;
-              gkq[e] = s2;
+        // Gram entries: 8 threads per item; items are the parent-path pairs
+        // (k_j.k_n, k_j.q_n for j = pj[e]) followed by the N diagonals k_n.q_n
+        {
+          const int npair = off[N];
+          const int items = npair + N;
+          const int sub = tid & 7;
+          for (int base = 0; base < items; base += kTcRowThreads / 8) {
+            const int item = base + (tid >> 3);
+            const bool act = item < items;
+            int j, n;
+            if (!act) {
+              j = 0, n = 0;
+            } else if (item < npair) {
+              j = pj[item];
+              n = 0;
+              while (off[n + 1] <= item) ++n;
+            } else {
+              j = item - npair, n = j;
+            }
+            float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int k = 4 * (sub + 8 * c);
+              const uint32_t oj = sw128_off(NC, j, k), on = sw128_off(NC, n, k),
+                             oq = sw128_off(NC, NMAX + n, k);
+              float4 kj = *reinterpret_cast<const float4 *>(Bhi + oj);
+              float4 t4 = *reinterpret_cast<const float4 *>(Blo + oj);
+              kj.x += t4.x, kj.y += t4.y, kj.z += t4.z, kj.w += t4.w;
+              float4 kn = *reinterpret_cast<const float4 *>(Bhi + on);
+              t4 = *reinterpret_cast<const float4 *>(Blo + on);
+              kn.x += t4.x, kn.y += t4.y, kn.z += t4.z, kn.w += t4.w;
+              float4 qn = *reinterpret_cast<const float4 *>(Bhi + oq);
+              t4 = *reinterpret_cast<const float4 *>(Blo + oq);
+              qn.x += t4.x, qn.y += t4.y, qn.z += t4.z, qn.w += t4.w;
+              s1 += dot4(kj, kn);
+              s2 += dot4(kj, qn);
+            }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) {
+              s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+              s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+            }
+            if (act && sub == 0) {
+              if (item < npair) {
+                gkk[item] = s1;
+                gkq[item] = s2;
+              } else {
+                kqn[j] = s2;
+              }
             }
           }
         }
@@ -345,11 +434,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
 
       // ================= per-tile preparation =================
-      for (int i = tid; i < N; i += kTcRowThreads) {
-        an[i] = bf2f(A.a[(lb * N + i) * Hv + h]);
-        bn[i] = bf2f(A.b[(lb * N + i) * Hv + h]);
+      if (tid < N) {
+        an[tid] = ga;
+        bn[tid] = gb;
       }
       ptx::named_sync(1, kTcRowThreads);
+      // per parent-path pair: g(j->p) times the Gram entries; gamma_p per node
       for (int i = tid; i < N; i += kTcRowThreads) {
         int j = par[i];
         float g = 1.f;
@@ -361,39 +451,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         gam[i] = g;
       }
-      // v of head h for all 128 rows (conv + SiLU), V[node][row]
-      {
-        constexpr int GV = kTcD / 8;
-        const int units = N * GV;
-        for (int u = tid; u < units; u += kTcRowThreads) {
-          const int i = u / GV, li = u % GV;
-          const int c0 = 2 * Hk * kTcD + h * kTcD + li * 8;
-          float v8[8];
-          conv8(v8, win + i * 4, K, x_lb, C, w_l, cache_s, c0);
-          float4 *dst = reinterpret_cast<float4 *>(V + i * kTcD + li * 8);
-          dst[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-          dst[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
-        }
-      }
-      ptx::named_sync(1, kTcRowThreads);
-      if (tid == 0) {
-        // accepted path: acc itself, then its parent path (coefficient g * a_acc)
-        int m = 0;
-        tj[m] = acc;
-        tg[m] = 1.f;
-        ++m;
-        int j = par[acc];
-        float g = an[acc];
-        for (int e = off[acc]; e < off[acc + 1]; ++e) {
-          tj[m] = pj[e];
-          tg[m] = g;
-          ++m;
-          g *= an[j];
-          j = par[j];
-        }
-        misc[4] = m;
-      }
-
       // ================= S0 -> tensor memory (tf32 hi / lo) =================
       if (!ptx::mbar_wait(&full_bar[s], (uint32_t)((it >> 1) & 1))) {
         if (A.status) *A.status = LBX_ETIMEOUT;
@@ -422,24 +479,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
-
-      // ================= conv-window persist =================
-      {
-        float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
-        if (tid < kTcD)
-          persist_conv_channel(2 * Hk * kTcD + h * kTcD + tid, K, C, crow, x_lb, cache_s, cache_o);
-        if (tid == 0) {
-          __threadfence();
-          unsigned int *cnt = A.counters + lb * Hk + kh;
-          const unsigned int prev = atomicAdd(cnt, 1u);
-          const int last = prev == (unsigned int)(G - 1);
-          if (last) {
-            atomicExch(cnt, 0u);
-            __threadfence();
-          }
-          misc[2] = last;
-        }
-      }
     }
     __syncthreads();  // ---------------------------------------------- S1
     if (misc[1]) break;
@@ -479,16 +518,115 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           pending = -1;
         }
+        // conv-window sources for this tile's persist work
+        window_sources(ccrow, K, acc, par_b);
+      }
+      // value-head window of the previous tile (its v conv finished before
+      // that tile's S3)
+      if (pv_x != nullptr) {
+        int ch[kTcD / 32];
+#pragma unroll
+        for (int i = 0; i < kTcD / 32; ++i) ch[i] = pv_c0 + lane + 32 * i;
+        persist_conv_batch(ch, K, C, pv_src, pv_x, pv_in, pv_out);
       }
       __syncwarp();
-    } else {
-      // q/k conv-window channels, by the last tile of the key-head group
-      if (misc[2]) {
-        float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
-        const int j = tid;  // 256 threads = 2 * 128 channels
-        persist_conv_channel(j < kTcD ? kh * kTcD + j : Hk * kTcD + kh * kTcD + (j - kTcD), K, C,
-                             crow, x_lb, cache_s, cache_o);
+      int src[LBX_MAX_CONV_WIDTH - 1];
+#pragma unroll
+      for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr) src[rr] = rr < K - 1 ? ccrow[rr] : 0;
+      // arrival: this CTA has finished reading the old q/k window of the
+      // key head (group prologue, before S1); the last of the G tiles of
+      // the group writes the new q/k window
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        unsigned int *cnt = A.counters + lb * Hk + kh;
+        const unsigned int prev = atomicAdd(cnt, 1u);
+        last = prev == (unsigned int)(G - 1);
+        if (last) {
+          atomicExch(cnt, 0u);
+          __threadfence();
+        }
       }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        int ch[2 * kTcD / 32];
+#pragma unroll
+        for (int i = 0; i < 2 * kTcD / 32; ++i) {
+          const int j = lane + 32 * i;
+          ch[i] = j < kTcD ? kh * kTcD + j : Hk * kTcD + kh * kTcD + (j - kTcD);
+        }
+        persist_conv_batch(ch, K, C, src, x_lb, cache_s, cache_o);
+      }
+      pv_x = x_lb, pv_in = cache_s, pv_out = cache_o, pv_c0 = 2 * Hk * kTcD + h * kTcD;
+#pragma unroll
+      for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr) pv_src[rr] = src[rr];
+    } else {
+      // ======== while the MMAs run: warp 0 builds T and W, the rest v ========
+      if (warp == 0) {
+        // T = (I + diag(b a) M)^-1, one column per lane, rows in node order;
+        // M[n][j] = g(j->p) k_j.k_n on the parent path of n.
+        const int m = lane;
+        for (int n = 0; n < N; ++n) {
+          const float d_n = bn[n] * an[n];
+          float tv = (m == n) ? 1.f : 0.f;
+          for (int e = off[n]; e < off[n + 1]; ++e) {
+            const float tjm = m < TP ? Tm[pj[e] * TP + m] : 0.f;
+            tv = fmaf(-d_n * ckk[e], tjm, tv);
+          }
+          if (m < TP) Tm[n * TP + m] = tv;
+          __syncwarp();
+        }
+        if (lane == 0) {
+          // accepted path: acc itself, then its parent path (coefficient g * a_acc)
+          int cnt = 0;
+          tj[cnt] = acc;
+          tg[cnt] = 1.f;
+          ++cnt;
+          int j = par[acc];
+          float g = an[acc];
+          for (int e = off[acc]; e < off[acc + 1]; ++e) {
+            tj[cnt] = pj[e];
+            tg[cnt] = g;
+            ++cnt;
+            g *= an[j];
+            j = par[j];
+          }
+          misc[4] = cnt;
+        }
+      } else {
+        // v of head h for all 128 rows (conv + SiLU), V[node][row]
+        constexpr int GV = kTcD / 8;
+        constexpr int NT = kTcRowThreads - 32;
+        constexpr int U = (NMAX * GV + NT - 1) / NT;
+        const int units = N * GV;
+        const int vt = tid - 32;
+#pragma unroll
+        for (int p = 0; p < U; ++p) {
+          const int u = p * NT + vt;
+          if (u < units) {
+            const int i = u / GV, li = u % GV;
+            float v8[8];
+            conv8(v8, win + i * 4, K, x_lb, C, w_l, cache_s, 2 * Hk * kTcD + h * kTcD + li * 8);
+            float4 *dst = reinterpret_cast<float4 *>(V + i * kTcD + li * 8);
+            dst[0] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+            dst[1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+          }
+        }
+      }
+      ptx::named_sync(1, kTcRowThreads);
+      // W = Q T, rows in parallel (warp per node): Q[n][j] = a_n g(j->p)
+      // k_j.q_n on the parent path, Q[n][n] = k_n.q_n
+      for (int n = warp; n < N; n += kTcRowThreads / 32) {
+        if (lane < TP) {
+          const float a_n = an[n];
+          float wv = kqn[n] * Tm[n * TP + lane];
+          for (int e = off[n]; e < off[n + 1]; ++e)
+            wv = fmaf(a_n * ckq[e], Tm[pj[e] * TP + lane], wv);
+          Wm[n * TP + lane] = wv;
+        }
+      }
+      ptx::named_sync(1, kTcRowThreads);
+
       // ================= accumulator row -> registers =================
       if (!ptx::mbar_wait(mma_bar, (uint32_t)(it & 1))) {
         if (A.status) *A.status = LBX_ETIMEOUT;
@@ -505,70 +643,99 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       ptx::tmem_wait_ld();
 
-      // ================= delta recurrence (one thread per row) =================
+      // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n ; delta = T rhs
+      float rhs[NMAX];
+#pragma unroll
+      for (int n = 0; n < NMAX; ++n)
+        rhs[n] = n < N ? bn[n] * fmaf(-an[n] * gam[n], dv[n], V[n * kTcD + r]) : 0.f;
       if (hf == 0) {
 #pragma unroll
         for (int n = 0; n < NMAX; ++n) {
           if (n < N) {
-            float u = gam[n] * dv[n];
-            for (int e = off[n]; e < off[n + 1]; ++e) u = fmaf(ckk[e], DEL[pj[e] * kTcD + r], u);
-            DEL[n * kTcD + r] = bn[n] * (V[n * kTcD + r] - an[n] * u);
+            float d = 0.f;
+#pragma unroll
+            for (int m4 = 0; m4 <= n / 4; ++m4) {
+              const float4 t4 = *reinterpret_cast<const float4 *>(Tm + n * TP + 4 * m4);
+              d = fmaf(t4.x, rhs[4 * m4], d);
+              if (4 * m4 + 1 <= n) d = fmaf(t4.y, rhs[4 * m4 + 1], d);
+              if (4 * m4 + 2 <= n) d = fmaf(t4.z, rhs[4 * m4 + 2], d);
+              if (4 * m4 + 3 <= n) d = fmaf(t4.w, rhs[4 * m4 + 3], d);
+            }
+            DEL[n * kTcD + r] = d;
+          }
+        }
+      } else {
+        // o_n = a_n gamma_p S0 q_n + (W rhs)_n
+        float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+          if (n < N) {
+            float ov = an[n] * gam[n] * dv[NMAX + n];
+#pragma unroll
+            for (int m4 = 0; m4 <= n / 4; ++m4) {
+              const float4 w4 = *reinterpret_cast<const float4 *>(Wm + n * TP + 4 * m4);
+              ov = fmaf(w4.x, rhs[4 * m4], ov);
+              if (4 * m4 + 1 <= n) ov = fmaf(w4.y, rhs[4 * m4 + 1], ov);
+              if (4 * m4 + 2 <= n) ov = fmaf(w4.z, rhs[4 * m4 + 2], ov);
+              if (4 * m4 + 3 <= n) ov = fmaf(w4.w, rhs[4 * m4 + 3], ov);
+            }
+            __stcs(o_base + (size_t)n * Hv * kTcD, ov);
           }
         }
       }
       ptx::named_sync(1, kTcRowThreads);
 
-      // ================= o_n = a_n (S_p q_n) + delta_n (k_n . q_n) =================
-      {
-        float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
-        auto emit = [&](int n, float sq) {
-          float u = gam[n] * sq;
-          for (int e = off[n]; e < off[n + 1]; ++e) u = fmaf(ckq[e], DEL[pj[e] * kTcD + r], u);
-          const float ov = fmaf(an[n], u, kqn[n] * DEL[n * kTcD + r]);
-          __stcs(o_base + (size_t)n * Hv * kTcD, ov);
-        };
-        if (hf == 0) {
-#pragma unroll
-          for (int n = 0; n < NMAX / 2; ++n)
-            if (n < N) emit(n, dv[NMAX + n]);
-        } else {
-#pragma unroll
-          for (int n = NMAX / 2; n < NMAX; ++n)
-            if (n < N) emit(n, dv[NMAX + n]);
-        }
-      }
-
       // ================= accepted state rows, in place =================
       {
         const int ntgt = misc[4];
         const float gacc = gam[acc] * an[acc];
-        for (int q = 0; q < 16; ++q) {
-          const int k = hf * 64 + 4 * q;
-          float4 *p = reinterpret_cast<float4 *>(st + sw128_off(kTcD, r, k));
-          float4 accv = f4_scale(gacc, *p);
-          for (int m = 0; m < ntgt; ++m) {
-            const int j = tj[m];
-            const float coef = tg[m] * DEL[j * kTcD + r];
-            const uint32_t ok = sw128_off(NC, j, k);
+        float4 accv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          accv[q] = f4_scale(gacc, *reinterpret_cast<const float4 *>(
+                                       st + sw128_off(kTcD, r, hf * 64 + 4 * q)));
+        for (int m = 0; m < ntgt; ++m) {
+          const int j = tj[m];
+          const float coef = tg[m] * DEL[j * kTcD + r];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t ok = sw128_off(NC, j, hf * 64 + 4 * q);
             float4 kj = *reinterpret_cast<const float4 *>(Bhi + ok);
             const float4 kl = *reinterpret_cast<const float4 *>(Blo + ok);
             kj.x += kl.x, kj.y += kl.y, kj.z += kl.z, kj.w += kl.w;
-            f4_fma(accv, coef, kj);
+            f4_fma(accv[q], coef, kj);
           }
-          *p = accv;
         }
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          *reinterpret_cast<float4 *>(st + sw128_off(kTcD, r, hf * 64 + 4 * q)) = accv[q];
+      }
+      // gates of the next tile
+      if (tid < N && it + 1 < count) {
+        const int t2 = t + 1, hg2 = t2 % G, rest2 = t2 / G, kh2 = rest2 % Hk, lb2 = rest2 / Hk;
+        ga = bf2f(A.a[((size_t)lb2 * N + tid) * Hv + kh2 * G + hg2]);
+        gb = bf2f(A.b[((size_t)lb2 * N + tid) * Hv + kh2 * G + hg2]);
       }
       ptx::fence_proxy_async();
       ptx::tc_fence_before();
     }
     __syncthreads();  // ---------------------------------------------- S3
     if (misc[1]) break;
-    if (ctrl_lane) {
-      const int row = tile_row(t);
-      for (int a = 0; a < 4; ++a)
-        ptx::tma_store_2d(&tmap_state, a * 32, row, st + a * (kStageBytes / 4));
-      ptx::bulk_commit();
+    if (is_ctrl) {
+      if (lane == 0) {
+        const int row = tile_row(t);
+        for (int a = 0; a < 4; ++a)
+          ptx::tma_store_2d(&tmap_state, a * 32, row, st + a * (kStageBytes / 4));
+        ptx::bulk_commit();
+      }
     }
+  }
+  // value-head window of the last tile
+  if (is_ctrl && pv_x != nullptr && !misc[1]) {
+    int ch[kTcD / 32];
+#pragma unroll
+    for (int i = 0; i < kTcD / 32; ++i) ch[i] = pv_c0 + lane + 32 * i;
+    persist_conv_batch(ch, K, C, pv_src, pv_x, pv_in, pv_out);
   }
 
   // ---- drain: outstanding loads (only after an abort) and stores ----
