@@ -2,6 +2,7 @@
 // mode, N <= 24): tensor map of the state, persistent grid of one CTA per SM.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "gdn_launch.h"
@@ -38,22 +39,39 @@ int sm_count() {
   return cache[dev];
 }
 
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base,
+               uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swz) {
+  const cuuint64_t gdim[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)inner * esize};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  return g_encode(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NMAX>
 int launch_tc(const StepArgs &A, cudaStream_t st) {
   if (!have_encode()) return LBX_ECUDA;
   const int nsm = sm_count();
   if (nsm <= 0) return LBX_ECUDA;
-  // the state viewed as a 2-D array [L * n_slots * Hv * 128 rows][128 fp32]
-  CUtensorMap map;
-  const cuuint64_t gdim[2] = {(cuuint64_t)kTcD,
-                              (cuuint64_t)A.L * A.n_slots * A.Hv * kTcD};
-  const cuuint64_t gstride[1] = {(cuuint64_t)kTcD * sizeof(float)};
-  const cuuint32_t box[2] = {32, 128};
-  const cuuint32_t estride[2] = {1, 1};
-  if (g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(A.state_in), gdim,
-               gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const int C = (2 * A.Hk + A.Hv) * kTcD;
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  // the state as [L * n_slots * Hv * 128 rows][128 fp32], 32-column boxes
+  if (!encode_2d(&maps.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A.state_in, kTcD,
+                 (uint64_t)A.L * A.n_slots * A.Hv * kTcD, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LBX_ECUDA;
+  // x as [L * Bq * N rows][C bf16]: one box = one 128-channel block of all nodes
+  if (!encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, A.x, C, (uint64_t)A.L * A.Bq * A.N,
+                 kTcD, A.N, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return LBX_ECUDA;
+  // the conv cache as [L * n_slots * (K-1) rows][C fp32]: one box = the K-1
+  // cached rows of a 128-channel block
+  if (A.K > 1 && !encode_2d(&maps.cache, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A.conv_cache, C,
+                            (uint64_t)A.L * A.n_slots * (A.K - 1), kTcD, A.K - 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
     return LBX_ECUDA;
   TcArgs T;
   T.s = A;
@@ -63,7 +81,7 @@ int launch_tc(const StepArgs &A, cudaStream_t st) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return LBX_ECUDA;
   const int grid = T.n_tiles < nsm ? T.n_tiles : nsm;
-  kern<<<grid, kTcThreads, smem, st>>>(map, T);
+  kern<<<grid, kTcThreads, smem, st>>>(maps, T);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
 
@@ -75,6 +93,7 @@ bool step_tc_supported(int d, int N, int chain) {
 
 int launch_step_tc(const StepArgs &A, cudaStream_t st) {
   if ((long long)A.L * A.n_slots * A.Hv * kTcD > 0x7fffffffLL) return LBX_EINVAL;
+  if ((long long)A.L * A.Bq * A.N > 0x7fffffffLL) return LBX_EINVAL;
   if (A.N <= 8) return launch_tc<8>(A, st);
   if (A.N <= 16) return launch_tc<16>(A, st);
   if (A.N <= 24) return launch_tc<24>(A, st);
