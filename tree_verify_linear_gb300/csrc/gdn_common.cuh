@@ -80,6 +80,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ float silu(float y) { return y / (1.0f + expf(-y)); }
+// SiLU through the hardware exponential and a fast divide (a few ulp; the
+// conv outputs it feeds are compared at ~1e-4 relative).
+__device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
 // Structural check of the whole batch, done by every CTA so that all CTAs
 // reach the same verdict without talking to each other.  Returns 0 or an

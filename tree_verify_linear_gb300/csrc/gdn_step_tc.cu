@@ -1,5 +1,6 @@
 // gdn_step_tc.cu -- host launch of the tensor-core fused step (d = 128, tree
-// mode, N <= 24): tensor map of the state, persistent grid of one CTA per SM.
+// mode, N <= 24): tensor maps of the state, the raw inputs and the conv cache;
+// persistent grid of two CTAs per SM.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -80,7 +81,11 @@ int launch_tc(const StepArgs &A, cudaStream_t st) {
   constexpr int smem = TcLayout<NMAX>::total;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return LBX_ECUDA;
-  const int grid = T.n_tiles < nsm ? T.n_tiles : nsm;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return LBX_ECUDA;
+  const int slots = kTcCtasPerSm * nsm;
+  const int grid = T.n_tiles < slots ? T.n_tiles : slots;
   kern<<<grid, kTcThreads, smem, st>>>(maps, T);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }

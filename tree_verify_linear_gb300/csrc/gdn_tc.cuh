@@ -1,37 +1,42 @@
 // gdn_tc.cuh -- fused tree-verify step on tensor cores (sm_103a, d = 128).
 //
-// Persistent kernel, one CTA per SM: 8 warps, two per TMEM lane quadrant,
-// splitting the 128 state columns; single lanes also issue the TMA copies
-// (thread 0) and the MMAs (thread 224).  The work is a list of tiles, one per (layer l,
-// request b, value head h) = one 128 x 128 fp32 state slab, ordered (l, b,
-// key head, head in group); every CTA takes a contiguous range, so consecutive
-// tiles usually share their key head and the q/k prologue is computed once
-// per key head per CTA.
+// Two CTAs share each SM (at most 113 KB of shared memory and 256 TMEM
+// columns each), so the latency-bound phases of one CTA overlap the other's.
+// A CTA has 4 warps, thread = state row = TMEM lane.  The work is a list of
+// tiles, one per (layer l, request b, value head h) = one 128 x 128 fp32 state
+// slab, ordered (l, b, key head, head in group); every CTA takes a contiguous
+// range, so consecutive tiles usually share their request and key head: the
+// tree tables are built once per request and the q/k prologue once per key
+// head.
 //
-// Everything a tile reads from global memory arrives by bulk-async copies
-// issued one tile ahead, on the stage's mbarrier: the state slab S0 (TMA,
-// four 32-column boxes, 128-byte swizzle, double-buffered), the raw inputs,
-// cached window rows and conv weights of the value head's channels
-// (double-buffered), and, when the next tile starts a new key head, those of
-// its q and k channels.  Per tile:
-//   * the row threads split S0 into bf16 hi + lo parts in tensor memory
-//     (operand A, lane = state row);
-//   * [k_0..k_{N-1} | q_0..q_{N-1}] (bf16 hi + lo, K-major, 128-byte swizzle)
-//     is operand B; three MMAs per K step (hi*hi + hi*lo + lo*hi, relative
-//     error ~2^-17) give S0 k_n and S0 q_n for every node in a TMEM
-//     accumulator;
-//   * the gated delta rule in closed form: with rhs_n = b_n v_n -
-//     b_n a_n gamma_p(n) S0 k_n, the deltas of a row are delta = T rhs where
-//     T = (I + diag(b a) M)^-1, M[n][j] = g(j->p(n)) k_j.k_n on the parent
-//     path (g = product of the gates strictly below j), and
-//     o = diag(a gamma) S0 q + W rhs with W = Q T, Q[n][j] = a_n g(j->p(n))
-//     k_j.q_n, Q[n][n] = k_n.q_n.  T and W are shared by the 128 rows and
-//     built level by level of the tree while the MMAs run;
-//   * the accepted state gamma_acc S0 + sum_{j in path(acc)} g(j->acc)
-//     delta_j k_j^T overwrites S0 in shared memory and goes back in place by
-//     TMA store.
+// Nodes are relabelled per request so that the accepted path comes first
+// (root = 0, ..., accepted node = P-1) and the rest follow in index order;
+// parents still precede children.  Global inputs arrive by bulk-async copies
+// issued by thread 0: the state slab S0 (TMA, four 32-column boxes, 128-byte
+// swizzle) into the stage, and the raw inputs, cached window rows and conv
+// weights of one 128-channel block at a time into the staging buffer (q then
+// k when a key head starts, then the value head's channels).
+//
+// With the factored delta rule S_n = gamma_n S0 + sum_{j in path(n)}
+// g(j->n) delta_j k_j^T (g = product of the gates strictly after j), every
+// delta of a row follows from rhs_n = b_n v_n - b_n a_n gamma_p(n) S0 k_n as
+// delta = T rhs, T = (I + diag(b a) M)^-1 with M[n][j] = g(j->p(n)) k_j.k_n
+// on the parent path, and o = diag(a gamma) S0 q + W rhs with W = Q T,
+// Q[n][j] = a_n g(j->p(n)) k_j.q_n, Q[n][n] = k_n.q_n.  Per tile, three
+// tensor-core products (bf16 hi + lo operands, three passes hi*hi + hi*lo +
+// lo*hi, relative error ~2^-17, fp32 accumulators in TMEM) do the row work:
+//   MMA1  [S0 k_n | S0 q_n]      = S0 [K | Q]^T      (A = S0 in TMEM, K = 128)
+//   MMA2  [delta_n | (W rhs)_n]  = rhs [T | W]^T     (A = rhs in TMEM, K = N)
+//   MMA3  sum_j c_j delta_j k_j^T = (c . delta) K     (A = path deltas, K = P,
+//         B = the first rows of operand K read N-major)
+// and the accepted state gamma_acc S0 + MMA3 is written straight to global
+// memory.  T and W (shared by the 128 rows) are built by one lane per
+// (node, ancestor-or-self) pair, each walking its stretch of the parent path,
+// with no barriers.  Loops over nodes are unrolled to the node capacity NMAX
+// and run without run-time guards: padding nodes carry zero gates, taps
+// beyond the conv width zero weights, every load a clamped, valid index.
 // The conv window of the slot is persisted in place: every value channel by
-// its row thread, and the q/k channels, by the CTA whose tile is the last of
+// its row thread, and the q/k channels by the CTA whose tile is the last of
 // its key-head group to arrive (arrival counter).
 #pragma once
 
@@ -44,16 +49,12 @@
 
 namespace lbx {
 
-constexpr int kTcD = 128;                       // head dimension of this kernel
-constexpr int kTcRowThreads = 256;              // 8 warps: two per TMEM lane quadrant
-constexpr int kTcThreads = kTcRowThreads;
-constexpr int kTcLoadThread = 0;                // issues the TMA copies
-constexpr int kTcMmaThread = 224;               // issues the MMAs
-constexpr int kTcArriveThread = 192;            // arrival counter
-constexpr uint32_t kTcTmemCols = 256;
-constexpr int kTcAHi = 0, kTcALo = 64, kTcD0 = 128;  // TMEM columns (A holds bf16 pairs)
-constexpr uint32_t kStageBytes = kTcD * kTcD * 4;    // one state slab, 64 KB
-constexpr int kTcMaxSmem = 227 * 1024;
+constexpr int kTcD = 128;                      // head dimension of this kernel
+constexpr int kTcThreads = 128;                // 4 warps, thread = state row
+constexpr int kTcCtasPerSm = 2;
+constexpr uint32_t kTcTmemCols = 256;          // per CTA: two CTAs fill the 512 columns
+constexpr uint32_t kStageBytes = kTcD * kTcD * 4;  // one state slab, 64 KB
+constexpr int kTcMaxSmem = 113 * 1024;             // two CTAs per SM
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -71,48 +72,57 @@ struct ConvStage {
 template <int NMAX>
 struct TcLayout {
   using CS = ConvStage<NMAX>;
-  static constexpr int NC = 2 * NMAX;               // B rows / accumulator columns
-  static constexpr int kB = NC * kTcD * 2;          // one of B hi / B lo (bf16)
+  static constexpr int NC = 2 * NMAX;                 // rows of [K | Q] and of [T | W]
+  static constexpr int KP = round_up(NMAX, 16);       // node dimension padded to the MMA K step
+  static constexpr int kB = NC * kTcD * 2;            // one of [K|Q] hi / lo (bf16, 128-byte swizzle)
+  static constexpr int kB2 = NC * KP * 2;             // one of [T|W] hi / lo (bf16, no swizzle)
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
-  static constexpr int TP = (NMAX + 3) & ~3;        // row pitch of T and W
-  static constexpr int stage0 = 0;
-  static constexpr int stage1 = stage0 + (int)kStageBytes;
-  static constexpr int bhi = stage1 + (int)kStageBytes;
+  static constexpr int TP = (NMAX + 3) & ~3;          // row pitch of the fp32 T scratch
+  // TMEM columns: S0 hi | lo, then [S0 k | S0 q], rhs or path deltas (hi | lo),
+  // [delta | W rhs]; the MMA3 accumulator reuses the S0 columns
+  static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + NC, cD2 = cA2 + KP;
+  static_assert(cD2 + NC <= kTcTmemCols, "tensor memory");
+  static constexpr int stage = 0;
+  static constexpr int bhi = stage + (int)kStageBytes;
   static constexpr int blo = bhi + kB;
-  static constexpr int kf = blo + kB;               // [NMAX][128] fp32 k rows
-  static constexpr int tm = kf + NMAX * kTcD * 4;   // [NMAX][TP] T
-  static constexpr int wm = tm + NMAX * TP * 4;     // [NMAX][TP] W
-  static constexpr int sv0 = round_up(wm + NMAX * TP * 4, 128);  // value-head inputs, 2 slots
-  static constexpr int sv1 = sv0 + CS::bytes;
-  static constexpr int sq = sv1 + CS::bytes;        // q inputs of the key head
-  static constexpr int sk = sq + CS::bytes;         // k inputs of the key head
-  static constexpr int pj = sk + CS::bytes;         // int   [kNPair] parent-path nodes
-  static constexpr int gkk = pj + 4 * kNPair;       // float [kNPair] k_j . k_n
-  static constexpr int gkq = gkk + 4 * kNPair;      // float [kNPair] k_j . q_n
-  static constexpr int ckk = gkq + 4 * kNPair;      // float [kNPair] g(j->p) k_j . k_n
-  static constexpr int ckq = ckk + 4 * kNPair;      // float [kNPair] g(j->p) k_j . q_n
-  static constexpr int par = ckq + 4 * kNPair;
-  static constexpr int off = par + 4 * NMAX;        // [NMAX + 4]
-  static constexpr int win = off + 4 * (NMAX + 4);  // [NMAX][4]
-  static constexpr int lvn = win + 16 * NMAX;       // nodes ordered by depth
-  static constexpr int lvo = lvn + 4 * NMAX;        // [NMAX + 4] level starts
-  static constexpr int an = lvo + 4 * (NMAX + 4);
+  static constexpr int b2hi = blo + kB;
+  static constexpr int b2lo = b2hi + kB2;
+  static constexpr int tf = b2lo + kB2;               // float [NMAX][TP] T scratch
+  static constexpr int stg = round_up(tf + NMAX * TP * 4, 128);  // conv-input staging
+  static constexpr int pj = stg + CS::bytes;          // uint8 [kNPair] parent-path nodes
+  static constexpr int gkk = pj + round_up(kNPair, 16);  // float [kNPair] k_j . k_n
+  static constexpr int gkq = gkk + 4 * kNPair;        // float [kNPair] k_j . q_n
+  static constexpr int porig = round_up(gkq + 4 * kNPair, 16);  // int [NMAX] parents, input labels
+  static constexpr int par = porig + 4 * NMAX;        // int [NMAX] parents, new labels
+  static constexpr int dep = par + 4 * NMAX;
+  static constexpr int off = dep + 4 * NMAX;          // [NMAX + 4] parent-path offsets
+  static constexpr int off2 = off + 4 * (NMAX + 4);   // [NMAX + 4] T/W lane offsets
+  static constexpr int win = off2 + 4 * (NMAX + 4);   // [NMAX][4] conv window sources (16-byte rows)
+  static constexpr int n2o = win + 16 * NMAX;         // new label -> input label
+  static constexpr int o2n = n2o + 4 * NMAX;          // input label -> new label
+  static constexpr int an = o2n + 4 * NMAX;
   static constexpr int bn = an + 4 * NMAX;
-  static constexpr int gam = bn + 4 * NMAX;
-  static constexpr int kqn = gam + 4 * NMAX;
-  static constexpr int tj = kqn + 4 * NMAX;         // accepted path nodes
-  static constexpr int tg = tj + 4 * NMAX;          // and their coefficients
-  static constexpr int crow = tg + 4 * NMAX;        // [4] new-window sources (row threads)
-  static constexpr int misc = crow + 16;            // ints, see kernel
-  static constexpr int bars = (misc + 64 + 7) & ~7; // 3 x uint64
+  static constexpr int gam = bn + 4 * NMAX;           // gamma of the parent
+  static constexpr int cpa = gam + 4 * NMAX;          // path coefficients g(j->acc)
+  static constexpr int kqn = cpa + 4 * NMAX;
+  static constexpr int crow = kqn + 4 * NMAX;         // [4] new-window sources
+  static constexpr int misc = crow + 16;              // ints, see kernel
+  static constexpr int bars = (misc + 64 + 7) & ~7;   // 3 x uint64
   static constexpr int total = bars + 3 * 8;
-  static_assert(kB % 1024 == 0, "operand B must keep 1024-byte alignment");
-  static_assert(total <= kTcMaxSmem, "shared memory");
+  static_assert(kB % 1024 == 0, "operand [K|Q] must keep 1024-byte alignment");
+  static_assert(total <= kTcMaxSmem, "two CTAs per SM");
+  static_assert(win % 16 == 0 && stg % 128 == 0 && b2hi % 16 == 0, "alignment");
 };
 
 struct TcArgs {
   StepArgs s;
   int n_tiles;  // L * Bq * Hv
+};
+
+struct TcMaps {
+  CUtensorMap state;  // [rows][128] fp32, box {32, 128}, 128-byte swizzle
+  CUtensorMap x;      // [L*Bq*N][C] bf16, box {128, N}
+  CUtensorMap cache;  // [L*n_slots*(K-1)][C] fp32, box {128, K-1} (K > 1)
 };
 
 // Byte offset of fp32 element (row, k) of a 128-column slab staged by TMA in
@@ -128,6 +138,12 @@ __device__ __forceinline__ uint32_t sw128_bf16(int rows, int row, int k) {
   const int atom = k >> 6, chunk = (k >> 3) & 7;
   return (uint32_t)(atom * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + ((k & 7) << 1));
 }
+// Byte offset of bf16 element (row, k) of a K-major operand with kp elements
+// per row, no swizzle: core matrices of 8 rows x 16 bytes, 128 bytes apart
+// along K, 8-row groups kp * 16 bytes apart.
+__device__ __forceinline__ uint32_t plain_bf16(int kp, int row, int k) {
+  return (uint32_t)((row >> 3) * kp * 16 + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
 
 // bf16 hi / lo split of x: hi = bf16(x), lo = bf16(x - hi).
 __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
@@ -136,21 +152,35 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) 
   hi = __bfloat16_as_ushort(h);
   lo = __bfloat16_as_ushort(l);
 }
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
-  return __uint_as_float(bits16 << 16);
+// The same for a pair, packed (a in the low half).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+// hi + lo of 8 consecutive elements of a row of operand [K | Q].
+__device__ __forceinline__ void operand_row8(const unsigned char *Bhi, const unsigned char *Blo,
+                                             uint32_t ofs, float (&v)[8]) {
+  float a[8], b[8];
+  unpack8(*reinterpret_cast<const uint4 *>(Bhi + ofs), a);
+  unpack8(*reinterpret_cast<const uint4 *>(Blo + ofs), b);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = a[e] + b[e];
 }
 
 // Conv-window sources of the persist: new row rr takes the (K-2-rr)-th
 // ancestor of acc, or old cache row depth(acc)+1+rr where the path is short.
-__device__ __forceinline__ void window_sources(int *dst, int K, int acc, const int32_t *par_b) {
+__device__ __forceinline__ void window_sources(int *dst, int K, int acc, const int *par) {
   int da = 0;
-  for (int m = acc; m > 0; m = par_b[m]) ++da;
+  for (int m = acc; m > 0; m = par[m]) ++da;
   for (int rr = 0; rr < K - 1; ++rr) {
     const int dist = K - 2 - rr;
     int w;
     if (dist <= da) {
       int m = acc;
-      for (int q = 0; q < dist; ++q) m = par_b[m];
+      for (int q = 0; q < dist; ++q) m = par[m];
       w = m;
     } else {
       w = -1 - (da + 1 + rr);
@@ -159,11 +189,12 @@ __device__ __forceinline__ void window_sources(int *dst, int K, int acc, const i
   }
 }
 
-// Conv + SiLU of 8 consecutive channels c0..c0+7 (within a staged block) of
-// one node whose window rows are win[0..4) (>= 0: staged x row; < 0: staged
-// cache row -1-w; taps j >= K carry weight 0).  Tap K-1 multiplies the node.
-// Loads use clamped, always-valid indices and the choice between the node
-// row and the cache row is a select, so the unrolled body has no branches.
+// Conv + SiLU of 8 consecutive channels c0..c0+7 (within the staged block)
+// of one node whose window rows are win[0..4) (>= 0: staged x row; < 0:
+// staged cache row -1-w; taps j >= K carry weight 0).  Tap K-1 multiplies the
+// node.  Loads use clamped, always-valid indices and the choice between the
+// node row and the cache row is a select, so the unrolled body has no
+// branches.
 template <int NMAX>
 __device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win, int K,
                                              const unsigned char *cs, int c0) {
@@ -191,82 +222,74 @@ __device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win, in
     }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) out[e] = silu(acc[e]);
+  for (int e = 0; e < 8; ++e) out[e] = silu_fast(acc[e]);
 }
 
-// New conv-window entries of staged channel c (global channel gc): row rr
-// takes src[rr] (>= 0: staged x row; < 0: staged old cache row -1-src).
-template <int NMAX>
-__device__ __forceinline__ void persist_staged(const unsigned char *cs, int c, int gc, int K,
-                                               int C, const int *src, float *cache_out) {
-  using CS = ConvStage<NMAX>;
+// New conv-window entries of channel gc, from global memory: row rr takes
+// src[rr] (>= 0: x row of the request; < 0: old cache row -1-src).  Every old
+// value is read before any is written (the window is updated in place).
+__device__ __forceinline__ void persist_channel_global(int gc, int K, int C, const int *src,
+                                                       const uint16_t *x_lb, const float *cache_in,
+                                                       float *cache_out) {
+  float val[LBX_MAX_CONV_WIDTH - 1];
 #pragma unroll
   for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
     if (rr < K - 1) {
       const int w = src[rr];
-      const float v =
-          w >= 0 ? bf2f(reinterpret_cast<const uint16_t *>(cs + CS::x)[w * kTcD + c])
-                 : reinterpret_cast<const float *>(cs + CS::c)[(-1 - w) * kTcD + c];
-      cache_out[(size_t)rr * C + gc] = v;
+      val[rr] = w >= 0 ? bf2f(x_lb[(size_t)w * C + gc]) : cache_in[(size_t)(-1 - w) * C + gc];
     }
+#pragma unroll
+  for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+    if (rr < K - 1) cache_out[(size_t)rr * C + gc] = val[rr];
 }
 
-struct TcMaps {
-  CUtensorMap state;  // [rows][128] fp32, box {32, 128}, 128-byte swizzle
-  CUtensorMap x;      // [L*Bq*N][C] bf16, box {128, N}
-  CUtensorMap cache;  // [L*n_slots*(K-1)][C] fp32, box {128, K-1} (K > 1)
-};
-
 template <int NMAX>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     gdn_step_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
-  constexpr int NC = Ly::NC;
-  constexpr int TP = Ly::TP;
+  constexpr int NC = Ly::NC, TP = Ly::TP, KP = Ly::KP, KH = KP / 2;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *stage[2] = {smem + Ly::stage0, smem + Ly::stage1};
-  unsigned char *svs[2] = {smem + Ly::sv0, smem + Ly::sv1};
-  unsigned char *sqs = smem + Ly::sq;
-  unsigned char *sks = smem + Ly::sk;
+  unsigned char *st = smem + Ly::stage;
+  unsigned char *sg = smem + Ly::stg;
   unsigned char *Bhi = smem + Ly::bhi;
   unsigned char *Blo = smem + Ly::blo;
-  float *Kf = reinterpret_cast<float *>(smem + Ly::kf);
-  float *Tm = reinterpret_cast<float *>(smem + Ly::tm);
-  float *Wm = reinterpret_cast<float *>(smem + Ly::wm);
-  int *pj = reinterpret_cast<int *>(smem + Ly::pj);
+  unsigned char *B2hi = smem + Ly::b2hi;
+  unsigned char *B2lo = smem + Ly::b2lo;
+  float *Tf = reinterpret_cast<float *>(smem + Ly::tf);
+  unsigned char *pj = smem + Ly::pj;
   float *gkk = reinterpret_cast<float *>(smem + Ly::gkk);
   float *gkq = reinterpret_cast<float *>(smem + Ly::gkq);
-  float *ckk = reinterpret_cast<float *>(smem + Ly::ckk);
-  float *ckq = reinterpret_cast<float *>(smem + Ly::ckq);
+  int *porig = reinterpret_cast<int *>(smem + Ly::porig);
   int *par = reinterpret_cast<int *>(smem + Ly::par);
+  int *dep = reinterpret_cast<int *>(smem + Ly::dep);
   int *off = reinterpret_cast<int *>(smem + Ly::off);
+  int *off2 = reinterpret_cast<int *>(smem + Ly::off2);
   int *win = reinterpret_cast<int *>(smem + Ly::win);
-  int *lvn = reinterpret_cast<int *>(smem + Ly::lvn);
-  int *lvo = reinterpret_cast<int *>(smem + Ly::lvo);
+  int *n2o = reinterpret_cast<int *>(smem + Ly::n2o);
+  int *o2n = reinterpret_cast<int *>(smem + Ly::o2n);
   float *an = reinterpret_cast<float *>(smem + Ly::an);
   float *bn = reinterpret_cast<float *>(smem + Ly::bn);
   float *gam = reinterpret_cast<float *>(smem + Ly::gam);
+  float *cpa = reinterpret_cast<float *>(smem + Ly::cpa);
   float *kqn = reinterpret_cast<float *>(smem + Ly::kqn);
-  int *tj = reinterpret_cast<int *>(smem + Ly::tj);
-  float *tg = reinterpret_cast<float *>(smem + Ly::tg);
   int *crow = reinterpret_cast<int *>(smem + Ly::crow);
   int *misc = reinterpret_cast<int *>(smem + Ly::misc);
   // misc[0] error flag, [1] abort, [2] last arriver, [3] TMEM base,
-  // [4] accepted-path length, [5] number of tree levels
-  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);  // [2]
-  uint64_t *mma_bar = full_bar + 2;
+  // [4] accepted-path length P, [5] number of T/W lanes
+  uint64_t *stage_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);
+  uint64_t *stg_bar = stage_bar + 1;
+  uint64_t *mma_bar = stage_bar + 2;
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const bool load_lane = tid == kTcLoadThread;
+  const int warp = tid >> 5;
+  const bool lead = tid == 0;  // issues the copies and the MMAs
   const int N = A.N, K = A.K, Hk = A.Hk, Hv = A.Hv, Bq = A.Bq;
   const int G = Hv / Hk;
   const int C = (2 * Hk + Hv) * kTcD;
-  const uint32_t x_bytes = (uint32_t)N * kTcD * 2;
-  const uint32_t c_bytes = (uint32_t)(K - 1) * kTcD * 4;
-  const uint32_t w_bytes = (uint32_t)kTcD * K * 2;
+  const uint32_t stg_bytes =
+      (uint32_t)N * kTcD * 2 + (uint32_t)(K - 1) * kTcD * 4 + (uint32_t)kTcD * K * 2;
 
   // ---- whole-batch validation (identical verdict in every CTA) ----
   {
@@ -289,8 +312,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
     misc[1] = 0;
-    ptx::mbar_init(&full_bar[0], 1);
-    ptx::mbar_init(&full_bar[1], 1);
+    ptx::mbar_init(stage_bar, 1);
+    ptx::mbar_init(stg_bar, 1);
     ptx::mbar_init(mma_bar, 1);
     ptx::fence_mbar_init();
   }
@@ -303,520 +326,580 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[3]);
 
-  // Issue every copy tile t needs into stage slot s (control thread): the
-  // state slab, the value-head conv inputs and, when `with_qk`, the q/k conv
-  // inputs of its key head.
-  auto issue_loads = [&](int t, int s, bool with_qk) {
-    const int hg = t % G, rest = t / G;
-    const int kh = rest % Hk, lbi = rest / Hk;
-    const int bq = lbi % Bq, l = lbi / Bq;
-    const int h = kh * G + hg;
-    const int srow = ((l * A.n_slots + A.slot[bq]) * Hv + h) * kTcD;
-    const int xrow = lbi * N;
-    const int crow0 = (l * A.n_slots + A.slot[bq]) * (K - 1);
-    const uint16_t *w_l = A.conv_w + (size_t)l * C * K;
-    const int nblk = with_qk ? 3 : 1;
-    const uint32_t bytes = kStageBytes + nblk * (x_bytes + c_bytes + w_bytes);
-    ptx::mbar_arrive_expect_tx(&full_bar[s], bytes);
+  // tile -> (head in group, key-head group, key head, layer*Bq + request,
+  // request, layer, value head)
+  struct Tile {
+    int hg, rest, kh, lbi, bq, l, h;
+  };
+  auto tile_of = [&](int t) {
+    Tile x;
+    x.hg = t % G;
+    x.rest = t / G;
+    x.kh = x.rest % Hk;
+    x.lbi = x.rest / Hk;
+    x.bq = x.lbi % Bq;
+    x.l = x.lbi / Bq;
+    x.h = x.kh * G + x.hg;
+    return x;
+  };
+  // lead thread: copies into the stage and the staging buffer
+  int n_state_loads = 0, n_stg_loads = 0;
+  auto load_state = [&](int t) {
+    const Tile x = tile_of(t);
+    const int srow = ((x.l * A.n_slots + A.slot[x.bq]) * Hv + x.h) * kTcD;
+    ptx::mbar_arrive_expect_tx(stage_bar, kStageBytes);
     for (int a = 0; a < 4; ++a)
-      ptx::tma_load_2d(stage[s] + a * (kStageBytes / 4), &maps.state, a * 32, srow, &full_bar[s]);
-    for (int blk = 0; blk < nblk; ++blk) {
-      unsigned char *dst = blk == 0 ? svs[s] : (blk == 1 ? sqs : sks);
-      const int ch0 = blk == 0 ? 2 * Hk * kTcD + h * kTcD
-                               : (blk == 1 ? kh * kTcD : Hk * kTcD + kh * kTcD);
-      ptx::tma_load_2d(dst + CS::x, &maps.x, ch0, xrow, &full_bar[s]);
-      if (K > 1) ptx::tma_load_2d(dst + CS::c, &maps.cache, ch0, crow0, &full_bar[s]);
-      ptx::bulk_load(dst + CS::w, w_l + (size_t)ch0 * K, w_bytes, &full_bar[s]);
+      ptx::tma_load_2d(st + a * (kStageBytes / 4), &maps.state, a * 32, srow, stage_bar);
+    ++n_state_loads;
+  };
+  // which: 0 = q, 1 = k, 2 = the value head's channels
+  auto load_block = [&](int t, int which) {
+    const Tile x = tile_of(t);
+    const int ch0 = which == 0 ? x.kh * kTcD
+                               : (which == 1 ? (Hk + x.kh) * kTcD : (2 * Hk + x.h) * kTcD);
+    const int crow0 = (x.l * A.n_slots + A.slot[x.bq]) * (K - 1);
+    ptx::mbar_arrive_expect_tx(stg_bar, stg_bytes);
+    ptx::tma_load_2d(sg + CS::x, &maps.x, ch0, x.lbi * N, stg_bar);
+    if (K > 1) ptx::tma_load_2d(sg + CS::c, &maps.cache, ch0, crow0, stg_bar);
+    ptx::bulk_load(sg + CS::w, A.conv_w + (size_t)x.l * C * K + (size_t)ch0 * K,
+                   (uint32_t)kTcD * K * 2, stg_bar);
+    ++n_stg_loads;
+  };
+  // phases waited for, the same count in every thread
+  uint32_t stg_waits = 0, mma_waits = 0;
+  auto wait_on = [&](uint64_t *bar, uint32_t &waits) {
+    if (!ptx::mbar_wait(bar, waits & 1u)) {
+      if (A.status) *A.status = LBX_ETIMEOUT;
+      atomicExch(&misc[1], 1);
     }
+    ++waits;
   };
 
-  int pending = -1;          // load thread: stage with an issued, unconsumed load
-  uint32_t pending_par = 0;
-  if (load_lane && count > 0) {
-    issue_loads(t_begin, 0, true);
-    pending = 0;
+  if (lead && count > 0) {
+    load_state(t_begin);
+    load_block(t_begin, 0);
   }
 
-  // row-thread identity: row r (TMEM lane), half hf (column half)
-  const int quad = warp & 3;
-  const int r = quad * 32 + lane;
-  const int hf = (warp >> 2) & 1;
-  const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+  const int r = tid;  // state row = TMEM lane
+  const uint32_t tq = tmem + ((uint32_t)(warp * 32) << 16);
 
-  // gates of the current tile, prefetched by threads tid < N
+  // gates of the current tile for input node tid (< N), prefetched
   float ga = 0.f, gb = 0.f;
   if (tid < N && count > 0) {
-    const int t = t_begin, hg = t % G, rest = t / G;
-    const size_t lbi = (size_t)(rest / Hk);
-    const int h = (rest % Hk) * G + hg;
-    ga = bf2f(A.a[(lbi * N + tid) * Hv + h]);
-    gb = bf2f(A.b[(lbi * N + tid) * Hv + h]);
+    const Tile x = tile_of(t_begin);
+    ga = bf2f(A.a[((size_t)x.lbi * N + tid) * Hv + x.h]);
+    gb = bf2f(A.b[((size_t)x.lbi * N + tid) * Hv + x.h]);
   }
 
-  int cur_group = -1;
+  int cur_req = -1, cur_group = -1;
   for (int it = 0; it < count; ++it) {
     const int t = t_begin + it;
-    const int s = it & 1;
-    const int hg = t % G, rest = t / G;
-    const int kh = rest % Hk, lbi = rest / Hk;
-    const int bq = lbi % Bq, l = lbi / Bq;
-    const int h = kh * G + hg;
-    const size_t lb = (size_t)lbi;
+    const Tile x = tile_of(t);
+    const int kh = x.kh, bq = x.bq, l = x.l, h = x.h;
+    const size_t lb = (size_t)x.lbi;
     const int slot_b = A.slot[bq];
     float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
-    const int32_t *par_b = A.parent + (size_t)bq * N;
-    const int acc = A.accepted[bq];
-    unsigned char *st = stage[s];
-    unsigned char *sv = svs[s];
 
-    {
-      // everything this tile reads from global memory
-      if (!ptx::mbar_wait(&full_bar[s], (uint32_t)((it >> 1) & 1))) {
-        if (A.status) *A.status = LBX_ETIMEOUT;
-        atomicExch(&misc[1], 1);
-      }
-      // ================= group prologue (new key head) =================
-      if (rest != cur_group) {
-        cur_group = rest;
-        for (int i = tid; i < NMAX; i += kTcRowThreads) {
-          // conv window rows; taps j >= K and padding nodes point at node 0
-          if (i < N) par[i] = par_b[i];
-          int m = i < N ? i : -2, past = 0;
-          for (int j = 0; j < 4; ++j) {
-            int w = 0;
-            if (i < N && j < K) {
-              if (m >= 0) {
-                w = m;
-                m = par_b[m];
-              } else {
-                ++past;
-                w = -1 - (K - 1 - past);
-              }
-            }
-            win[i * 4 + j] = w;
-          }
-        }
-        // T and W rows of padding nodes stay zero
-        for (int idx = N * TP + tid; idx < NMAX * TP; idx += kTcRowThreads) {
-          Tm[idx] = 0.f;
-          Wm[idx] = 0.f;
-        }
-        if (tid == 32) window_sources(crow, K, acc, par_b);
-        ptx::named_sync(1, kTcRowThreads);
-        if (tid == 0) {
-          // depth per node (parents precede children), parent-path offsets,
-          // and the nodes grouped by depth
-          int dep[NMAX];
-          int nlev = 0;
-          off[0] = 0;
-          for (int i = 0; i < N; ++i) {
-            dep[i] = i == 0 ? 0 : dep[par[i]] + 1;
-            off[i + 1] = off[i] + dep[i];
-            nlev = dep[i] + 1 > nlev ? dep[i] + 1 : nlev;
-          }
-          int pos = 0;
-          for (int d = 0; d < nlev; ++d) {
-            lvo[d] = pos;
-            for (int i = 0; i < N; ++i)
-              if (dep[i] == d) lvn[pos++] = i;
-          }
-          lvo[nlev] = pos;
-          misc[5] = nlev;
-        }
-        ptx::named_sync(1, kTcRowThreads);
-        for (int i = tid; i < N; i += kTcRowThreads) {
-          int j = par[i];
-          for (int e = off[i]; e < off[i + 1]; ++e) {
-            pj[e] = j;
-            j = par[j];
-          }
-        }
-        // q/k conv + SiLU + L2 from the staged inputs -> operand B rows
-        // (bf16 hi / lo), k rows also in fp32; q scaled
-        {
-          constexpr int GQ = kTcD / 8;  // 16 threads per (node, q|k)
-          constexpr int U = (2 * NMAX * GQ + kTcRowThreads - 1) / kTcRowThreads;
-          const int units = 2 * N * GQ;
-#pragma unroll
-          for (int p = 0; p < U; ++p) {
-            const int u = p * kTcRowThreads + tid;
-            const bool act = u < units;
-            const int grp = act ? u / GQ : 0, li = u % GQ;
-            const bool is_q = grp >= N;
-            const int i = is_q ? grp - N : grp;
-            float v8[8];
-            if (act) {
-              conv8_staged<NMAX>(v8, win + i * 4, K, is_q ? sqs : sks, li * 8);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = 0.f;
-            }
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
-#pragma unroll
-            for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (act) {
-              const float scale = rsqrtf(ss + A.l2_eps) * (is_q ? A.q_scale : 1.f);
-              const int brow = is_q ? NMAX + i : i;
-              float vv[8];
-              uint32_t wh[4], wl[4];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) vv[e] = scale * v8[e];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                uint16_t h0, l0, h1, l1;
-                split_bf16(vv[2 * e], h0, l0);
-                split_bf16(vv[2 * e + 1], h1, l1);
-                wh[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                wl[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-              }
-              const uint32_t o = sw128_bf16(NC, brow, li * 8);
-              *reinterpret_cast<uint4 *>(Bhi + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-              *reinterpret_cast<uint4 *>(Blo + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-              if (!is_q) {
-                float4 *kd = reinterpret_cast<float4 *>(Kf + i * kTcD + li * 8);
-                kd[0] = make_float4(vv[0], vv[1], vv[2], vv[3]);
-                kd[1] = make_float4(vv[4], vv[5], vv[6], vv[7]);
-              }
-            }
-          }
-          // zero the unused rows of operand B
-          const int pad_rows = 2 * (NMAX - N);
-          for (int idx = tid; idx < pad_rows * 16; idx += kTcRowThreads) {
-            const int pr = idx / 16, q = idx % 16;
-            const int brow = pr < NMAX - N ? N + pr : NMAX + N + (pr - (NMAX - N));
-            const uint32_t o = sw128_bf16(NC, brow, 8 * q);
-            *reinterpret_cast<uint4 *>(Bhi + o) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4 *>(Blo + o) = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        ptx::fence_proxy_async();
-        ptx::named_sync(1, kTcRowThreads);
-        // Gram entries, 8 threads per item: the parent-path pairs (k_j.k_n
-        // and k_j.q_n for j = pj[e]) followed by the N diagonals k_n.q_n
-        {
-          const int npair = off[N];
-          const int items = npair + N;
-          const int sub = tid & 7;
-          for (int base = 0; base < items; base += kTcRowThreads / 8) {
-            const int item = base + (tid >> 3);
-            const bool act = item < items;
-            int j = 0, n = 0;
-            if (act) {
-              if (item < npair) {
-                j = pj[item];
-                while (off[n + 1] <= item) ++n;
-              } else {
-                j = n = item - npair;
-              }
-            }
-            float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int k = 8 * (sub + 8 * c);  // 8 consecutive elements
-              const float4 *kj = reinterpret_cast<const float4 *>(Kf + j * kTcD + k);
-              const float4 *kn = reinterpret_cast<const float4 *>(Kf + n * kTcD + k);
-              const uint4 qh = *reinterpret_cast<const uint4 *>(Bhi + sw128_bf16(NC, NMAX + n, k));
-              const uint4 ql = *reinterpret_cast<const uint4 *>(Blo + sw128_bf16(NC, NMAX + n, k));
-              const uint32_t hw[4] = {qh.x, qh.y, qh.z, qh.w}, lw[4] = {ql.x, ql.y, ql.z, ql.w};
-              float qv[8];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                qv[2 * e] = bf16_bits_to_f32(hw[e] & 0xffffu) + bf16_bits_to_f32(lw[e] & 0xffffu);
-                qv[2 * e + 1] = bf16_bits_to_f32(hw[e] >> 16) + bf16_bits_to_f32(lw[e] >> 16);
-              }
-              const float4 j0 = kj[0], j1 = kj[1], n0 = kn[0], n1 = kn[1];
-              s1 += dot4(j0, n0) + dot4(j1, n1);
-              s2 += dot4(j0, make_float4(qv[0], qv[1], qv[2], qv[3])) +
-                    dot4(j1, make_float4(qv[4], qv[5], qv[6], qv[7]));
-            }
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) {
-              s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-              s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-            }
-            if (act && sub == 0) {
-              if (item < npair) {
-                gkk[item] = s1;
-                gkq[item] = s2;
-              } else {
-                kqn[j] = s2;
-              }
-            }
-          }
-        }
-        ptx::named_sync(1, kTcRowThreads);
-      }
-
-      // ================= per-tile gates and pair coefficients =================
+    // ================= request prologue: tree tables =================
+    if (bq != cur_req) {
+      cur_req = bq;
+      const int32_t *par_b = A.parent + (size_t)bq * N;
+      const int acc = A.accepted[bq];
       if (tid < NMAX) {
-        an[tid] = tid < N ? ga : 0.f;
-        bn[tid] = tid < N ? gb : 0.f;
-        if (tid >= N) gam[tid] = 0.f;
+        porig[tid] = tid < N ? par_b[tid] : -1;
+        o2n[tid] = -1;
       }
-      ptx::named_sync(1, kTcRowThreads);
-      for (int i = tid; i < N; i += kTcRowThreads) {
+      // [T | W] entries outside the (node, ancestor-or-self) pairs stay zero
+      for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
+        *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
+      ptx::named_sync(1, kTcThreads);
+      if (tid == 0) {
+        // the accepted path, root first, takes labels 0..P-1; the other
+        // nodes follow in input order
+        int P = 0;
+        for (int m = acc; m >= 0; m = porig[m]) ++P;
+        int p = P;
+        for (int m = acc; m >= 0; m = porig[m]) {
+          --p;
+          n2o[p] = m;
+          o2n[m] = p;
+        }
+        int c = P;
+        for (int i = 0; i < N; ++i)
+          if (o2n[i] < 0) {
+            n2o[c] = i;
+            o2n[i] = c;
+            ++c;
+          }
+        misc[4] = P;
+      }
+      if (tid == 32) window_sources(crow, K, acc, porig);
+      ptx::named_sync(1, kTcThreads);
+      if (tid < NMAX) {
+        // parent, depth and conv window rows in the new labels; taps j >= K
+        // and padding nodes point at input row 0
+        const int o = tid < N ? n2o[tid] : 0;
+        par[tid] = tid < N && porig[o] >= 0 ? o2n[porig[o]] : -1;
+        int d = 0;
+        if (tid < N)
+          for (int m = porig[o]; m >= 0; m = porig[m]) ++d;
+        dep[tid] = d;
+        int m = tid < N ? o : -2, past = 0;
+        for (int j = 0; j < 4; ++j) {
+          int w = 0;
+          if (tid < N && j < K) {
+            if (m >= 0) {
+              w = m;
+              m = porig[m];
+            } else {
+              ++past;
+              w = -1 - (K - 1 - past);
+            }
+          }
+          win[tid * 4 + j] = w;
+        }
+      }
+      ptx::named_sync(1, kTcThreads);
+      if (tid <= NMAX) {
+        int o1 = 0, o2 = 0;
+        for (int i = 0; i < N && i < tid; ++i) {
+          o1 += dep[i];
+          o2 += dep[i] + 1;
+        }
+        off[tid] = o1;
+        off2[tid] = o2;
+      }
+      ptx::named_sync(1, kTcThreads);
+      for (int i = tid; i < N; i += kTcThreads) {
         int j = par[i];
-        float g = 1.f;
         for (int e = off[i]; e < off[i + 1]; ++e) {
-          ckk[e] = g * gkk[e];
-          ckq[e] = g * gkq[e];
-          g *= an[j];
+          pj[e] = (unsigned char)j;
           j = par[j];
         }
-        gam[i] = g;
       }
-      if (tid == 64) {
-        // accepted path: acc itself, then its parent path (coefficient g * a_acc)
-        int cnt = 0;
-        tj[cnt] = acc;
-        tg[cnt] = 1.f;
-        ++cnt;
-        int j = par[acc];
-        float g = an[acc];
-        while (j >= 0) {
-          tj[cnt] = j;
-          tg[cnt] = g;
-          ++cnt;
-          g *= an[j];
-          j = par[j];
-        }
-        misc[4] = cnt;
-      }
-
-      // ================= S0 -> tensor memory (bf16 hi / lo) =================
-      {
-        uint32_t vh[32], vl[32];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 x4 =
-              *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, hf * 64 + 4 * q));
-          uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
-          split_bf16(x4.x, h0, l0);
-          split_bf16(x4.y, h1, l1);
-          split_bf16(x4.z, h2, l2);
-          split_bf16(x4.w, h3, l3);
-          vh[2 * q] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-          vh[2 * q + 1] = (uint32_t)h2 | ((uint32_t)h3 << 16);
-          vl[2 * q] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-          vl[2 * q + 1] = (uint32_t)l2 | ((uint32_t)l3 << 16);
-        }
-        ptx::tmem_st32(tq + kTcAHi + hf * 32, vh);
-        ptx::tmem_st32(tq + kTcALo + hf * 32, vl);
-        ptx::tmem_wait_st();
-      }
-      ptx::tc_fence_before();
+      if (tid == 0) misc[5] = off2[N];
+      ptx::named_sync(1, kTcThreads);
     }
+
+    // ================= group prologue (new key head) =================
+    if (x.rest != cur_group) {
+      cur_group = x.rest;
+      // q, then k: conv + SiLU + L2 from the staged inputs -> operand rows
+      // (bf16 hi / lo); q scaled
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        wait_on(stg_bar, stg_waits);
+        constexpr int GQ = kTcD / 8;  // 16 threads per node
+        constexpr int U = (NMAX * GQ + kTcThreads - 1) / kTcThreads;
+        const int units = N * GQ;
+#pragma unroll
+        for (int p = 0; p < U; ++p) {
+          const int u = p * kTcThreads + tid;
+          const bool act = u < units;
+          const int i = act ? u / GQ : 0, li = u % GQ;
+          float v8[8];
+          conv8_staged<NMAX>(v8, win + i * 4, K, sg, li * 8);
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
+#pragma unroll
+          for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          if (act) {
+            const float scale = rsqrtf(ss + A.l2_eps) * (which == 0 ? A.q_scale : 1.f);
+            const int brow = which == 0 ? NMAX + i : i;
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              split_bf16x2(scale * v8[2 * e], scale * v8[2 * e + 1], wh[e], wl[e]);
+            const uint32_t ob = sw128_bf16(NC, brow, li * 8);
+            *reinterpret_cast<uint4 *>(Bhi + ob) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4 *>(Blo + ob) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          }
+        }
+        // zero the padding rows of this half of the operand
+        for (int idx = tid; idx < (NMAX - N) * 16; idx += kTcThreads) {
+          const int brow = (which == 0 ? NMAX : 0) + N + idx / 16;
+          const uint32_t ob = sw128_bf16(NC, brow, 8 * (idx % 16));
+          *reinterpret_cast<uint4 *>(Bhi + ob) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(Blo + ob) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::named_sync(1, kTcThreads);  // staging consumed
+        if (lead) load_block(t, which == 0 ? 1 : 2);
+      }
+      ptx::fence_proxy_async();
+      // Gram entries, 8 threads per item: the parent-path pairs (k_j.k_n and
+      // k_j.q_n for j = pj[e]) followed by the N diagonals k_n.q_n
+      {
+        const int npair = off[N];
+        const int items = npair + N;
+        const int sub = tid & 7;
+        for (int base = 0; base < items; base += kTcThreads / 8) {
+          const int item = base + (tid >> 3);
+          const bool act = item < items;
+          int j = 0, n = 0;
+          if (act) {
+            if (item < npair) {
+              j = pj[item];
+              while (off[n + 1] <= item) ++n;
+            } else {
+              j = n = item - npair;
+            }
+          }
+          float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int k = 8 * (sub + 8 * c);  // 8 consecutive elements
+            float kj[8], kn[8], qn[8];
+            operand_row8(Bhi, Blo, sw128_bf16(NC, j, k), kj);
+            operand_row8(Bhi, Blo, sw128_bf16(NC, n, k), kn);
+            operand_row8(Bhi, Blo, sw128_bf16(NC, NMAX + n, k), qn);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              s1 = fmaf(kj[e], kn[e], s1);
+              s2 = fmaf(kj[e], qn[e], s2);
+            }
+          }
+#pragma unroll
+          for (int o = 4; o > 0; o >>= 1) {
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+          }
+          if (act && sub == 0) {
+            if (item < npair) {
+              gkk[item] = s1;
+              gkq[item] = s2;
+            } else {
+              kqn[j] = s2;
+            }
+          }
+        }
+      }
+    }
+
+    // ================= per-tile gates, T and W =================
+    if (tid < NMAX && tid >= N) {
+      an[tid] = 0.f;
+      bn[tid] = 0.f;
+      gam[tid] = 0.f;
+    }
+    if (tid < N) {
+      const int nn = o2n[tid];
+      an[nn] = ga;
+      bn[nn] = gb;
+    }
+    ptx::named_sync(1, kTcThreads);
+    const int P = misc[4];
+    {
+      // one lane per (node n, ancestor-or-self m): column m of T along the
+      // stretch m -> n of the parent path (positions 0..L), then W[n][m]
+      const int nl = misc[5];
+      for (int lane_id = tid; lane_id < nl; lane_id += kTcThreads) {
+        int n = 0;
+        while (off2[n + 1] <= lane_id) ++n;
+        const int L = lane_id - off2[n];
+        const int e0 = off[n];
+        const int m = L == 0 ? n : pj[e0 + L - 1];
+        Tf[m * TP + m] = 1.f;
+        float xl = 1.f;
+        for (int p = 1; p <= L; ++p) {
+          const int jp = p == L ? n : pj[e0 + (L - p - 1)];
+          const int ep = off[jp];
+          float s = 0.f, g = 1.f;
+          for (int q = p - 1; q >= 0; --q) {
+            const int e = ep + (p - q - 1);
+            const int jq = pj[e];
+            s = fmaf(g * gkk[e], Tf[jq * TP + m], s);
+            g *= an[jq];
+          }
+          xl = -bn[jp] * an[jp] * s;
+          Tf[jp * TP + m] = xl;
+        }
+        float s = 0.f, g = 1.f;
+        for (int q = L - 1; q >= 0; --q) {
+          const int e = e0 + (L - q - 1);
+          const int jq = pj[e];
+          s = fmaf(g * gkq[e], Tf[jq * TP + m], s);
+          g *= an[jq];
+        }
+        const float wv = fmaf(kqn[n], xl, an[n] * s);
+        if (L == dep[n]) gam[n] = g;  // product of the gates of all ancestors
+        uint16_t th, tl, wh, wl;
+        split_bf16(xl, th, tl);
+        split_bf16(wv, wh, wl);
+        *reinterpret_cast<uint16_t *>(B2hi + plain_bf16(KP, n, m)) = th;
+        *reinterpret_cast<uint16_t *>(B2lo + plain_bf16(KP, n, m)) = tl;
+        *reinterpret_cast<uint16_t *>(B2hi + plain_bf16(KP, NMAX + n, m)) = wh;
+        *reinterpret_cast<uint16_t *>(B2lo + plain_bf16(KP, NMAX + n, m)) = wl;
+      }
+      // accepted-path coefficients g(j->acc) for path nodes j = 0..P-1
+      if (tid < NMAX) {
+        float c = tid < P ? 1.f : 0.f;
+        for (int u = tid + 1; u < P; ++u) c *= an[u];
+        cpa[tid] = c;
+      }
+    }
+    ptx::fence_proxy_async();
+
+    // ================= S0 -> tensor memory (bf16 hi / lo) =================
+    if (!ptx::mbar_wait(stage_bar, (uint32_t)(it & 1))) {
+      if (A.status) *A.status = LBX_ETIMEOUT;
+      atomicExch(&misc[1], 1);
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t vh[32], vl[32];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 x4 =
+            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, half * 64 + 4 * q));
+        split_bf16x2(x4.x, x4.y, vh[2 * q], vl[2 * q]);
+        split_bf16x2(x4.z, x4.w, vh[2 * q + 1], vl[2 * q + 1]);
+      }
+      ptx::tmem_st32(tq + Ly::cA1 + half * 32, vh);
+      ptx::tmem_st32(tq + Ly::cA1 + 64 + half * 32, vl);
+    }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S1
     if (misc[1]) break;
 
-    if (tid == kTcMmaThread) {
-      // D = S0 [K|Q]^T: three bf16 passes (hi*hi, hi*lo, lo*hi) over K = 128
+    if (lead) {
+      // MMA1: [S0 k | S0 q] = S0 [K|Q]^T, three passes over K = 128
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_bf16(128, NC);
       const uint32_t bhi_a = ptx::smem_u32(Bhi), blo_a = ptx::smem_u32(Blo);
       uint32_t accum = 0;
 #pragma unroll 1
       for (int pass = 0; pass < 3; ++pass) {
-        const uint32_t a_col = pass == 2 ? kTcALo : kTcAHi;
+        const uint32_t a_col = Ly::cA1 + (pass == 2 ? 64 : 0);
         const uint32_t b_base = pass == 1 ? blo_a : bhi_a;
 #pragma unroll
         for (int ks = 0; ks < kTcD / 16; ++ks) {
           const uint32_t baddr = b_base + (uint32_t)((ks >> 2) * (NC * 128) + (ks & 3) * 32);
-          ptx::mma_bf16_ts(tmem + kTcD0, tmem + a_col + 8 * ks, ptx::sdesc_sw128(baddr), idesc,
+          ptx::mma_bf16_ts(tmem + Ly::cD1, tmem + a_col + 8 * ks, ptx::sdesc_sw128(baddr), idesc,
                            accum);
           accum = 1;
         }
       }
       ptx::mma_commit(mma_bar);
     }
-    if (tid == kTcArriveThread) {
-      // arrival: this CTA has finished reading the old q/k window of the key
-      // head (group prologue, before S1); the last of the G tiles of the
-      // group writes the new q/k window
-      __threadfence();
-      unsigned int *cnt = A.counters + lb * Hk + kh;
-      const unsigned int prev = atomicAdd(cnt, 1u);
-      const int last = prev == (unsigned int)(G - 1);
-      if (last) {
-        atomicExch(cnt, 0u);
-        __threadfence();
-      }
-      misc[2] = last;
-    }
-    if (load_lane) pending = -1;
-    __syncwarp();
+    // arrival: this CTA has finished reading the old q/k window of the key
+    // head (its TMA copy completed before S1); the last of the G tiles of
+    // the group writes the new one.  The result is used after the v conv.
+    unsigned int arrived = 0;
+    unsigned int *cnt = A.counters + lb * Hk + kh;
+    if (tid == 32) arrived = atomicAdd(cnt, 1u);
+
+    // ================= v of this row for every node (staged inputs) =================
+    wait_on(stg_bar, stg_waits);
+    float vv[NMAX];
     {
-      // ======== while the MMAs run: T by tree levels, W, this row's v ========
-      {
-        const int nlev = misc[5];
-        for (int d = 0; d < nlev; ++d) {
-          for (int idx = lvo[d] + warp; idx < lvo[d + 1]; idx += kTcRowThreads / 32) {
-            const int n = lvn[idx];
-            if (lane < TP) {
-              const float dn = bn[n] * an[n];
-              float tv = lane == n ? 1.f : 0.f;
-              for (int e = off[n]; e < off[n + 1]; ++e)
-                tv = fmaf(-dn * ckk[e], Tm[pj[e] * TP + lane], tv);
-              Tm[n * TP + lane] = tv;
-            }
-          }
-          ptx::named_sync(1, kTcRowThreads);
-        }
-        for (int n = warp; n < N; n += kTcRowThreads / 32) {
-          if (lane < TP) {
-            const float a_n = an[n];
-            float wv = kqn[n] * Tm[n * TP + lane];
-            for (int e = off[n]; e < off[n + 1]; ++e)
-              wv = fmaf(a_n * ckq[e], Tm[pj[e] * TP + lane], wv);
-            Wm[n * TP + lane] = wv;
-          }
-        }
-      }
-      // v_n of this row for every node (conv + SiLU of channel r, staged);
-      // padding nodes and taps read valid rows with weight 0 / gate 0
-      float vv[NMAX];
-      {
-        const uint16_t *xs = reinterpret_cast<const uint16_t *>(sv + CS::x);
-        const float *cs = reinterpret_cast<const float *>(sv + CS::c);
-        const uint16_t *ws = reinterpret_cast<const uint16_t *>(sv + CS::w) + r * K;
-        float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
+      const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
+      const float *cs = reinterpret_cast<const float *>(sg + CS::c);
+      const uint16_t *ws = reinterpret_cast<const uint16_t *>(sg + CS::w) + r * K;
+      float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
 #pragma unroll
-        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
-          wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
+      for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
+        wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
 #pragma unroll
-        for (int n = 0; n < NMAX; ++n) {
-          float y = 0.f;
+      for (int n = 0; n < NMAX; ++n) {
+        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * n);
+        const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
+        float y = 0.f;
 #pragma unroll
-          for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
-            const int w = win[n * 4 + j];
-            const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
-            const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
-            y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
-          }
-          vv[n] = silu(y);
+        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
+          const int w = wj[j];
+          const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
+          const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
+          y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
         }
+        vv[n] = silu_fast(y);
       }
       // this row's value channel of the conv window (only this tile reads it)
-      if (hf == 0) persist_staged<NMAX>(sv, r, 2 * Hk * kTcD + h * kTcD + r, K, C, crow, cache_o);
-      ptx::named_sync(1, kTcRowThreads);
-      if (misc[2]) {
-        // new q/k window of the key head, from the staged q/k inputs
-        const int c = tid & (kTcD - 1);
-        if (tid < kTcD) persist_staged<NMAX>(sqs, c, kh * kTcD + c, K, C, crow, cache_o);
-        else persist_staged<NMAX>(sks, c, Hk * kTcD + kh * kTcD + c, K, C, crow, cache_o);
-      }
-      ptx::named_sync(1, kTcRowThreads);
-      if (load_lane && it + 1 < count) {
-        // next tile's copies, into the other stage once its previous contents
-        // (tile it-1) have been read by their TMA store; the staged q/k
-        // inputs are free now
-        const int s2 = (it + 1) & 1;
-        ptx::bulk_wait_read_all();
-        issue_loads(t + 1, s2, (t + 1) / G != rest);
-        pending = s2;
-        pending_par = (uint32_t)(((it + 1) >> 1) & 1);
-      }
+#pragma unroll
+      for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+        if (rr < K - 1) {
+          const int w = crow[rr];
+          const float v = w >= 0 ? bf2f(xs[w * kTcD + r]) : cs[(-1 - w) * kTcD + r];
+          cache_o[(size_t)rr * C + (2 * Hk + h) * kTcD + r] = v;
+        }
+    }
+    if (tid == 32) {
+      const int last = arrived == (unsigned int)(G - 1);
+      if (last) atomicExch(cnt, 0u);
+      misc[2] = last;
+    }
+    ptx::named_sync(1, kTcThreads);  // staging consumed; misc[2] visible
+    if (lead && it + 1 < count) {
+      // next tile's first staging block: its q inputs if it starts a new key
+      // head, else its value-head inputs
+      load_block(t + 1, (t + 1) / G != x.rest ? 0 : 2);
+    }
+    if (misc[2]) {
+      // new q/k window of the key head (this CTA's tile arrived last)
+      const uint16_t *x_lb = A.x + lb * N * C;
+      const float *cache_s = A.conv_cache + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
+      persist_channel_global(kh * kTcD + r, K, C, crow, x_lb, cache_s, cache_o);
+      persist_channel_global((Hk + kh) * kTcD + r, K, C, crow, x_lb, cache_s, cache_o);
+    }
 
-      // ================= accumulator row -> registers =================
-      if (!ptx::mbar_wait(mma_bar, (uint32_t)(it & 1))) {
-        if (A.status) *A.status = LBX_ETIMEOUT;
-        atomicExch(&misc[1], 1);
-      }
-      ptx::tc_fence_after();
+    // ================= rhs -> tensor memory =================
+    wait_on(mma_bar, mma_waits);
+    ptx::tc_fence_after();
+    float oq[NMAX];
+    {
       float dv[NC];
 #pragma unroll
       for (int c = 0; c < NC / 16; ++c) {
         float t16[16];
-        ptx::tmem_ld16(tq + kTcD0 + 16 * c, t16);
+        ptx::tmem_ld16(tq + Ly::cD1 + 16 * c, t16);
 #pragma unroll
         for (int e = 0; e < 16; ++e) dv[16 * c + e] = t16[e];
       }
       ptx::tmem_wait_ld();
-
-      // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n ; delta = T rhs ; (hf 1) o
-      float rhs[NMAX];  // padding nodes have b = 0, so rhs = 0
+      // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
+      float rhs[KP];
 #pragma unroll
-      for (int n = 0; n < NMAX; ++n) rhs[n] = bn[n] * fmaf(-an[n] * gam[n], dv[n], vv[n]);
-      float dl[NMAX];
-      {
-        float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
-#pragma unroll
-        for (int n = 0; n < NMAX; ++n) {
-          float d = 0.f;
-#pragma unroll
-          for (int m4 = 0; m4 <= n / 4; ++m4) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(Tm + n * TP + 4 * m4);
-            const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (4 * m4 + e <= n) d = fmaf(tt[e], rhs[4 * m4 + e], d);
-          }
-          dl[n] = d;
-          if (hf == 1) {
-            float ov = an[n] * gam[n] * dv[NMAX + n];
-#pragma unroll
-            for (int m4 = 0; m4 <= n / 4; ++m4) {
-              const float4 w4 = *reinterpret_cast<const float4 *>(Wm + n * TP + 4 * m4);
-              const float ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (4 * m4 + e <= n) ov = fmaf(ww[e], rhs[4 * m4 + e], ov);
-            }
-            if (n < N) __stcs(o_base + (size_t)n * Hv * kTcD, ov);
-          }
+      for (int n = 0; n < KP; ++n) {
+        if (n < NMAX) {
+          const float ag = an[n] * gam[n];
+          rhs[n] = bn[n] * fmaf(-ag, dv[n], vv[n]);
+          oq[n] = ag * dv[NMAX + n];
+        } else {
+          rhs[n] = 0.f;
         }
       }
-
-      // ================= accepted state row, in place (this half) =================
-      {
-        const int ntgt = misc[4];
-        const float gacc = gam[acc] * an[acc];
-        float4 accv[16];
+      uint32_t rh[KH], rl[KH];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          accv[q] = f4_scale(gacc, *reinterpret_cast<const float4 *>(
-                                       st + sw128_f32(kTcD, r, hf * 64 + 4 * q)));
-        for (int m = 0; m < ntgt; ++m) {
-          const int j = tj[m];
-          float dj = 0.f;
-#pragma unroll
-          for (int n = 0; n < NMAX; ++n) dj = (j == n) ? dl[n] : dj;
-          const float coef = tg[m] * dj;
-          const float4 *kr = reinterpret_cast<const float4 *>(Kf + j * kTcD + hf * 64);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) f4_fma(accv[q], coef, kr[q]);
-        }
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          *reinterpret_cast<float4 *>(st + sw128_f32(kTcD, r, hf * 64 + 4 * q)) = accv[q];
+      for (int e = 0; e < KH; ++e) split_bf16x2(rhs[2 * e], rhs[2 * e + 1], rh[e], rl[e]);
+      if constexpr (KH == 16) {
+        ptx::tmem_st16(tq + Ly::cA2, rh);
+        ptx::tmem_st16(tq + Ly::cA2 + KH, rl);
+      } else {
+        ptx::tmem_st8(tq + Ly::cA2, rh);
+        ptx::tmem_st8(tq + Ly::cA2 + KH, rl);
       }
-      // gates of the next tile
-      if (tid < N && it + 1 < count) {
-        const int t2 = t + 1, hg2 = t2 % G, rest2 = t2 / G;
-        const size_t lb2 = (size_t)(rest2 / Hk);
-        const int h2 = (rest2 % Hk) * G + hg2;
-        ga = bf2f(A.a[(lb2 * N + tid) * Hv + h2]);
-        gb = bf2f(A.b[(lb2 * N + tid) * Hv + h2]);
-      }
-      ptx::fence_proxy_async();
-      ptx::tc_fence_before();
     }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    __syncthreads();  // ---------------------------------------------- S2
+    if (misc[1]) break;
+    if (lead) {
+      // MMA2: [delta | W rhs] = rhs [T|W]^T, three passes over K = KP
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_bf16(128, NC);
+      const uint32_t b2h = ptx::smem_u32(B2hi), b2l = ptx::smem_u32(B2lo);
+      uint32_t accum = 0;
+#pragma unroll 1
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t a_col = Ly::cA2 + (pass == 2 ? KH : 0);
+        const uint32_t b_base = pass == 1 ? b2l : b2h;
+#pragma unroll
+        for (int ks = 0; ks < KP / 16; ++ks) {
+          ptx::mma_bf16_ts(tmem + Ly::cD2, tmem + a_col + 8 * ks,
+                           ptx::sdesc(b_base + 256u * ks, 128u, (uint32_t)KP * 16u, 0u), idesc,
+                           accum);
+          accum = 1;
+        }
+      }
+      ptx::mma_commit(mma_bar);
+    }
+
+    // ================= o, path deltas -> tensor memory =================
+    wait_on(mma_bar, mma_waits);
+    ptx::tc_fence_after();
+    {
+      float d2[NC];
+#pragma unroll
+      for (int c = 0; c < NC / 16; ++c) {
+        float t16[16];
+        ptx::tmem_ld16(tq + Ly::cD2 + 16 * c, t16);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) d2[16 * c + e] = t16[e];
+      }
+      ptx::tmem_wait_ld();
+      float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
+#pragma unroll
+      for (int n = 0; n < NMAX; ++n)
+        if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[n] + d2[NMAX + n]);
+      float dl[KP];
+#pragma unroll
+      for (int n = 0; n < KP; ++n) dl[n] = n < NMAX ? cpa[n] * d2[n] : 0.f;
+      uint32_t dh[KH], dlo[KH];
+#pragma unroll
+      for (int e = 0; e < KH; ++e) split_bf16x2(dl[2 * e], dl[2 * e + 1], dh[e], dlo[e]);
+      if constexpr (KH == 16) {
+        ptx::tmem_st16(tq + Ly::cA2, dh);
+        ptx::tmem_st16(tq + Ly::cA2 + KH, dlo);
+      } else {
+        ptx::tmem_st8(tq + Ly::cA2, dh);
+        ptx::tmem_st8(tq + Ly::cA2 + KH, dlo);
+      }
+    }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S3
     if (misc[1]) break;
-    if (load_lane) {
-      const int row = ((l * A.n_slots + slot_b) * Hv + h) * kTcD;
-      for (int a = 0; a < 4; ++a)
-        ptx::tma_store_2d(&maps.state, a * 32, row, st + a * (kStageBytes / 4));
-      ptx::bulk_commit();
+    if (lead) {
+      // MMA3: sum_j c_j delta_j k_j^T over the path rows of operand K,
+      // read N-major, three passes over K = KP
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kTcD);
+      const uint32_t bhi_a = ptx::smem_u32(Bhi), blo_a = ptx::smem_u32(Blo);
+      uint32_t accum = 0;
+#pragma unroll 1
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t a_col = Ly::cA2 + (pass == 2 ? KH : 0);
+        const uint32_t b_base = pass == 1 ? blo_a : bhi_a;
+#pragma unroll
+        for (int ks = 0; ks < KP / 16; ++ks) {
+          ptx::mma_bf16_ts(tmem + Ly::cA1, tmem + a_col + 8 * ks,
+                           ptx::sdesc(b_base + 2048u * ks, (uint32_t)NC * 128u, 1024u, 2u), idesc,
+                           accum);
+          accum = 1;
+        }
+      }
+      ptx::mma_commit(mma_bar);
     }
+    // gates of the next tile
+    if (tid < N && it + 1 < count) {
+      const Tile x2 = tile_of(t + 1);
+      ga = bf2f(A.a[((size_t)x2.lbi * N + tid) * Hv + x2.h]);
+      gb = bf2f(A.b[((size_t)x2.lbi * N + tid) * Hv + x2.h]);
+    }
+
+    // ================= accepted state row -> global memory =================
+    wait_on(mma_bar, mma_waits);
+    ptx::tc_fence_after();
+    {
+      const float gacc = gam[P - 1] * an[P - 1];
+      float4 *srow = reinterpret_cast<float4 *>(
+          A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD);
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float d32[32];
+        ptx::tmem_ld32(tq + Ly::cA1 + 32 * c4, d32);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 s4 =
+              *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, 32 * c4 + 4 * q));
+          srow[8 * c4 + q] = make_float4(fmaf(gacc, s4.x, d32[4 * q]), fmaf(gacc, s4.y, d32[4 * q + 1]),
+                                         fmaf(gacc, s4.z, d32[4 * q + 2]),
+                                         fmaf(gacc, s4.w, d32[4 * q + 3]));
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();  // ---------------------------------------------- S4
+    if (misc[1]) break;
+    if (lead && it + 1 < count) load_state(t + 1);  // the stage has been read
   }
 
-  // ---- drain: an outstanding load (only after an abort) and the stores ----
-  if (load_lane) {
-    if (pending >= 0 && misc[1]) (void)ptx::mbar_wait(&full_bar[pending], pending_par);
-    ptx::bulk_wait_all();
+  // ---- drain: copies still in flight after an abort ----
+  if (lead && misc[1]) {
+    if (n_state_loads > 0) (void)ptx::mbar_wait(stage_bar, (uint32_t)((n_state_loads - 1) & 1));
+    if (n_stg_loads > 0) (void)ptx::mbar_wait(stg_bar, (uint32_t)((n_stg_loads - 1) & 1));
   }
   ptx::tc_fence_before();
   __syncthreads();
