@@ -78,7 +78,7 @@ int launch_tc(const StepArgs &A, cudaStream_t st) {
   T.s = A;
   T.n_tiles = A.L * A.Bq * A.Hv;
   auto kern = gdn_step_tc_kernel<NMAX>;
-  constexpr int smem = TcLayout<NMAX>::total;
+  constexpr int smem = TcLayout<NMAX>::smem_bytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return LBX_ECUDA;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -73,19 +73,21 @@ template <int NMAX>
 struct TcLayout {
   using CS = ConvStage<NMAX>;
   static constexpr int NC = 2 * NMAX;                 // rows of [K | Q] and of [T | W]
+  static constexpr int R1 = 2 * NC;                   // [K|Q] hi rows, then [K|Q] lo rows
   static constexpr int KP = round_up(NMAX, 16);       // node dimension padded to the MMA K step
-  static constexpr int kB = NC * kTcD * 2;            // one of [K|Q] hi / lo (bf16, 128-byte swizzle)
+  static constexpr int kB = R1 * kTcD * 2;            // [K|Q] hi and lo (bf16, 128-byte swizzle)
   static constexpr int kB2 = NC * KP * 2;             // one of [T|W] hi / lo (bf16, no swizzle)
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
   static constexpr int TP = (NMAX + 3) & ~3;          // row pitch of the fp32 T scratch
-  // TMEM columns: S0 hi | lo, then [S0 k | S0 q], rhs or path deltas (hi | lo),
-  // [delta | W rhs]; the MMA3 accumulator reuses the S0 columns
-  static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + NC, cD2 = cA2 + KP;
-  static_assert(cD2 + NC <= kTcTmemCols, "tensor memory");
+  // TMEM columns: S0 hi | lo; the two halves of [S0 k | S0 q] (hi-row and
+  // lo-row products); rhs or path deltas (hi | lo).  [delta | W rhs] reuses
+  // the first half of the MMA1 accumulator, the Gram product and the MMA3
+  // accumulator the S0 columns.
+  static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + R1, cD2 = cD1;
+  static_assert(cA2 + KP <= kTcTmemCols, "tensor memory");
   static constexpr int stage = 0;
-  static constexpr int bhi = stage + (int)kStageBytes;
-  static constexpr int blo = bhi + kB;
-  static constexpr int b2hi = blo + kB;
+  static constexpr int b1 = stage + (int)kStageBytes;
+  static constexpr int b2hi = b1 + kB;
   static constexpr int b2lo = b2hi + kB2;
   static constexpr int tf = b2lo + kB2;               // float [NMAX][TP] T scratch
   static constexpr int stg = round_up(tf + NMAX * TP * 4, 128);  // conv-input staging
@@ -109,9 +111,16 @@ struct TcLayout {
   static constexpr int misc = crow + 16;              // ints, see kernel
   static constexpr int bars = (misc + 64 + 7) & ~7;   // 3 x uint64
   static constexpr int total = bars + 3 * 8;
+  // The Gram product reads A = 128 rows of the [K|Q] operand per K step
+  // (rows past the K rows feed accumulator lanes that are not used): the
+  // last byte it can touch is 16 KB past the start of the second 64-column
+  // atom of the lo rows.  The allocation covers that range.
+  static constexpr int gram_extent = b1 + NC * 128 + R1 * 128 + 128 * 128;
+  static constexpr int smem_bytes = total > gram_extent ? total : gram_extent;
   static_assert(kB % 1024 == 0, "operand [K|Q] must keep 1024-byte alignment");
-  static_assert(total <= kTcMaxSmem, "two CTAs per SM");
+  static_assert(smem_bytes <= kTcMaxSmem, "two CTAs per SM");
   static_assert(win % 16 == 0 && stg % 128 == 0 && b2hi % 16 == 0, "alignment");
+  static_assert(NMAX * NC * 4 <= 2 * kB2, "the Gram matrix is staged in the [T|W] buffer");
 };
 
 struct TcArgs {
@@ -160,16 +169,6 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uin
   hi = *reinterpret_cast<const uint32_t *>(&h);
   lo = *reinterpret_cast<const uint32_t *>(&l);
 }
-// hi + lo of 8 consecutive elements of a row of operand [K | Q].
-__device__ __forceinline__ void operand_row8(const unsigned char *Bhi, const unsigned char *Blo,
-                                             uint32_t ofs, float (&v)[8]) {
-  float a[8], b[8];
-  unpack8(*reinterpret_cast<const uint4 *>(Bhi + ofs), a);
-  unpack8(*reinterpret_cast<const uint4 *>(Blo + ofs), b);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) v[e] = a[e] + b[e];
-}
-
 // Conv-window sources of the persist: new row rr takes the (K-2-rr)-th
 // ancestor of acc, or old cache row depth(acc)+1+rr where the path is short.
 __device__ __forceinline__ void window_sources(int *dst, int K, int acc, const int *par) {
@@ -189,23 +188,39 @@ __device__ __forceinline__ void window_sources(int *dst, int K, int acc, const i
   }
 }
 
-// Conv + SiLU of 8 consecutive channels c0..c0+7 (within the staged block)
-// of one node whose window rows are win[0..4) (>= 0: staged x row; < 0:
-// staged cache row -1-w; taps j >= K carry weight 0).  Tap K-1 multiplies the
-// node.  Loads use clamped, always-valid indices and the choice between the
-// node row and the cache row is a select, so the unrolled body has no
-// branches.
+// Weights of 8 consecutive channels c0..c0+7 of a staged block, by window
+// element: wsl[e][j] multiplies the j-th element of the window (tap K-1-j),
+// 0 for j >= K.
 template <int NMAX>
-__device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win, int K,
-                                             const unsigned char *cs, int c0) {
+__device__ __forceinline__ void conv_weights8(float (&wsl)[8][LBX_MAX_CONV_WIDTH], int K,
+                                              const unsigned char *cs, int c0) {
   using CS = ConvStage<NMAX>;
   const uint16_t *ws = reinterpret_cast<const uint16_t *>(cs + CS::w);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
+      wsl[e][j] = j < K ? bf2f(ws[(c0 + e) * K + (K - 1 - j >= 0 ? K - 1 - j : 0)]) : 0.f;
+}
+
+// Conv + SiLU of 8 consecutive channels c0..c0+7 (within the staged block)
+// of one node whose window rows are win[0..4) (>= 0: staged x row; < 0:
+// staged cache row -1-w).  Loads use clamped, always-valid indices and the
+// choice between the node row and the cache row is a select, so the unrolled
+// body has no branches.
+template <int NMAX>
+__device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win,
+                                             const float (&wsl)[8][LBX_MAX_CONV_WIDTH],
+                                             const unsigned char *cs, int c0) {
+  using CS = ConvStage<NMAX>;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const int4 w4 = *reinterpret_cast<const int4 *>(win);
+  const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
   for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
-    const int row = win[j];
+    const int row = wj[j];
     const int xr = row >= 0 ? row : 0;
     const int cr = row >= 0 ? 0 : -1 - row;
     float xn[8];
@@ -213,16 +228,19 @@ __device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win, in
     const float4 *cp = reinterpret_cast<const float4 *>(cs + CS::c + cr * kTcD * 4 + c0 * 4);
     const float4 lo = cp[0], hi = cp[1];
     const float xc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    const int tap = K - 1 - j >= 0 ? K - 1 - j : 0;
-    const float on = j < K ? 1.f : 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float wv = on * bf2f(ws[(c0 + e) * K + tap]);
-      acc[e] = fmaf(wv, row >= 0 ? xn[e] : xc[e], acc[e]);
-    }
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wsl[e][j], row >= 0 ? xn[e] : xc[e], acc[e]);
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) out[e] = silu_fast(acc[e]);
+}
+
+// 32-byte store of 8 floats (32-byte aligned address).
+__device__ __forceinline__ void stg_v8(float *p, float v0, float v1, float v2, float v3, float v4,
+                                       float v5, float v6, float v7) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v0),
+               "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7)
+               : "memory");
 }
 
 // New conv-window entries of channel gc, from global memory: row rr takes
@@ -243,18 +261,45 @@ __device__ __forceinline__ void persist_channel_global(int gc, int K, int C, con
     if (rr < K - 1) cache_out[(size_t)rr * C + gc] = val[rr];
 }
 
+// Product with B = [K|Q] (hi rows 0..NC-1, lo rows NC..2NC-1, K = 128,
+// 128-byte swizzle) and a bf16 hi / lo operand A over the same K: pass 1,
+// A_hi x [B_hi | B_lo] (N = 2 NC), initialises 2 NC accumulator columns and
+// pass 2, A_lo x B_hi, adds into the first NC; column n of the result is the
+// sum of columns n and NC + n.  A is in TMEM (S0: hi columns a, lo columns
+// a + 64) or, when A_SMEM, the K rows of B itself (hi rows, then lo rows).
+template <int NMAX, bool A_SMEM>
+__device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t a, uint32_t b1) {
+  using Ly = TcLayout<NMAX>;
+  constexpr int NC = Ly::NC, R1 = Ly::R1;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const uint32_t idesc = pass == 0 ? ptx::idesc_bf16(128, 2 * NC) : ptx::idesc_bf16(128, NC);
+#pragma unroll
+    for (int ks = 0; ks < kTcD / 16; ++ks) {
+      const uint32_t koff = (uint32_t)((ks >> 2) * (R1 * 128) + (ks & 3) * 32);
+      const uint64_t bdesc = ptx::sdesc_sw128(b1 + koff);
+      const uint32_t acc = (pass | ks) != 0;
+      if constexpr (A_SMEM) {
+        const uint32_t abase = a + (pass == 1 ? (uint32_t)NC * 128u : 0u);
+        ptx::mma_bf16_ss(d_tmem, ptx::sdesc_sw128(abase + koff), bdesc, idesc, acc);
+      } else {
+        ptx::mma_bf16_ts(d_tmem, a + (pass == 1 ? 64u : 0u) + 8u * ks, bdesc, idesc, acc);
+      }
+    }
+  }
+}
+
 template <int NMAX>
 __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     gdn_step_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
-  constexpr int NC = Ly::NC, TP = Ly::TP, KP = Ly::KP, KH = KP / 2;
+  constexpr int NC = Ly::NC, R1 = Ly::R1, TP = Ly::TP, KP = Ly::KP, KH = KP / 2;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *st = smem + Ly::stage;
   unsigned char *sg = smem + Ly::stg;
-  unsigned char *Bhi = smem + Ly::bhi;
-  unsigned char *Blo = smem + Ly::blo;
+  unsigned char *B1 = smem + Ly::b1;  // [K|Q] hi rows 0..NC-1, lo rows NC..2NC-1
   unsigned char *B2hi = smem + Ly::b2hi;
   unsigned char *B2lo = smem + Ly::b2lo;
   float *Tf = reinterpret_cast<float *>(smem + Ly::tf);
@@ -489,16 +534,20 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         wait_on(stg_bar, stg_waits);
-        constexpr int GQ = kTcD / 8;  // 16 threads per node
+        constexpr int GQ = kTcD / 8;  // 16 threads per node, the same 8 channels for every node
         constexpr int U = (NMAX * GQ + kTcThreads - 1) / kTcThreads;
+        static_assert(kTcThreads % GQ == 0, "channel group fixed per thread");
         const int units = N * GQ;
+        const int li = tid % GQ;
+        float wsl[8][LBX_MAX_CONV_WIDTH];
+        conv_weights8<NMAX>(wsl, K, sg, li * 8);
 #pragma unroll
         for (int p = 0; p < U; ++p) {
           const int u = p * kTcThreads + tid;
           const bool act = u < units;
-          const int i = act ? u / GQ : 0, li = u % GQ;
+          const int i = act ? u / GQ : 0;
           float v8[8];
-          conv8_staged<NMAX>(v8, win + i * 4, K, sg, li * 8);
+          conv8_staged<NMAX>(v8, win + i * 4, wsl, sg, li * 8);
           float ss = 0.f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
@@ -511,69 +560,77 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               split_bf16x2(scale * v8[2 * e], scale * v8[2 * e + 1], wh[e], wl[e]);
-            const uint32_t ob = sw128_bf16(NC, brow, li * 8);
-            *reinterpret_cast<uint4 *>(Bhi + ob) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4 *>(Blo + ob) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, li * 8)) =
+                make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, li * 8)) =
+                make_uint4(wl[0], wl[1], wl[2], wl[3]);
           }
         }
         // zero the padding rows of this half of the operand
         for (int idx = tid; idx < (NMAX - N) * 16; idx += kTcThreads) {
           const int brow = (which == 0 ? NMAX : 0) + N + idx / 16;
-          const uint32_t ob = sw128_bf16(NC, brow, 8 * (idx % 16));
-          *reinterpret_cast<uint4 *>(Bhi + ob) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4 *>(Blo + ob) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, 8 * (idx % 16))) =
+              make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, 8 * (idx % 16))) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
         ptx::named_sync(1, kTcThreads);  // staging consumed
         if (lead) load_block(t, which == 0 ? 1 : 2);
       }
+      // Gram matrix K [K|Q]^T on the tensor cores (A = the K rows of the
+      // operand, read from shared memory; rows >= NMAX of the product are
+      // not used), staged as fp32 [NMAX][NC] in the [T|W] buffer
       ptx::fence_proxy_async();
-      // Gram entries, 8 threads per item: the parent-path pairs (k_j.k_n and
-      // k_j.q_n for j = pj[e]) followed by the N diagonals k_n.q_n
+      ptx::tc_fence_before();
+      ptx::named_sync(1, kTcThreads);
+      if (lead) {
+        ptx::tc_fence_after();
+        mma_kq<NMAX, true>(tmem + Ly::cA1, ptx::smem_u32(B1), ptx::smem_u32(B1));
+        ptx::mma_commit(mma_bar);
+      }
+      wait_on(mma_bar, mma_waits);
+      ptx::tc_fence_after();
+      float *Gm = reinterpret_cast<float *>(B2hi);
+      if (warp == 0) {
+        float g[R1];
+#pragma unroll
+        for (int c = 0; c < R1 / 32; ++c) {
+          float t32[32];
+          ptx::tmem_ld32(tq + Ly::cA1 + 32 * c, t32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) g[32 * c + e] = t32[e];
+        }
+        ptx::tmem_wait_ld();
+        if (tid < NMAX) {
+#pragma unroll
+          for (int n4 = 0; n4 < NC / 4; ++n4)
+            *reinterpret_cast<float4 *>(Gm + tid * NC + 4 * n4) =
+                make_float4(g[4 * n4] + g[NC + 4 * n4], g[4 * n4 + 1] + g[NC + 4 * n4 + 1],
+                            g[4 * n4 + 2] + g[NC + 4 * n4 + 2], g[4 * n4 + 3] + g[NC + 4 * n4 + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::named_sync(1, kTcThreads);
       {
+        // parent-path pairs (k_j.k_n, k_j.q_n for j = pj[e]), then the
+        // diagonals k_n.q_n
         const int npair = off[N];
-        const int items = npair + N;
-        const int sub = tid & 7;
-        for (int base = 0; base < items; base += kTcThreads / 8) {
-          const int item = base + (tid >> 3);
-          const bool act = item < items;
-          int j = 0, n = 0;
-          if (act) {
-            if (item < npair) {
-              j = pj[item];
-              while (off[n + 1] <= item) ++n;
-            } else {
-              j = n = item - npair;
-            }
-          }
-          float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int k = 8 * (sub + 8 * c);  // 8 consecutive elements
-            float kj[8], kn[8], qn[8];
-            operand_row8(Bhi, Blo, sw128_bf16(NC, j, k), kj);
-            operand_row8(Bhi, Blo, sw128_bf16(NC, n, k), kn);
-            operand_row8(Bhi, Blo, sw128_bf16(NC, NMAX + n, k), qn);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              s1 = fmaf(kj[e], kn[e], s1);
-              s2 = fmaf(kj[e], qn[e], s2);
-            }
-          }
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) {
-            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-          }
-          if (act && sub == 0) {
-            if (item < npair) {
-              gkk[item] = s1;
-              gkq[item] = s2;
-            } else {
-              kqn[j] = s2;
-            }
+        for (int item = tid; item < npair + N; item += kTcThreads) {
+          if (item < npair) {
+            int n = 0;
+            while (off[n + 1] <= item) ++n;
+            const int j = pj[item];
+            gkk[item] = Gm[j * NC + n];
+            gkq[item] = Gm[j * NC + NMAX + n];
+          } else {
+            const int n = item - npair;
+            kqn[n] = Gm[n * NC + NMAX + n];
           }
         }
       }
+      ptx::named_sync(1, kTcThreads);
+      for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
+        *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
     }
 
     // ================= per-tile gates, T and W =================
@@ -664,23 +721,9 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     if (misc[1]) break;
 
     if (lead) {
-      // MMA1: [S0 k | S0 q] = S0 [K|Q]^T, three passes over K = 128
+      // MMA1: [S0 k | S0 q] = S0 [K|Q]^T over K = 128
       ptx::tc_fence_after();
-      constexpr uint32_t idesc = ptx::idesc_bf16(128, NC);
-      const uint32_t bhi_a = ptx::smem_u32(Bhi), blo_a = ptx::smem_u32(Blo);
-      uint32_t accum = 0;
-#pragma unroll 1
-      for (int pass = 0; pass < 3; ++pass) {
-        const uint32_t a_col = Ly::cA1 + (pass == 2 ? 64 : 0);
-        const uint32_t b_base = pass == 1 ? blo_a : bhi_a;
-#pragma unroll
-        for (int ks = 0; ks < kTcD / 16; ++ks) {
-          const uint32_t baddr = b_base + (uint32_t)((ks >> 2) * (NC * 128) + (ks & 3) * 32);
-          ptx::mma_bf16_ts(tmem + Ly::cD1, tmem + a_col + 8 * ks, ptx::sdesc_sw128(baddr), idesc,
-                           accum);
-          accum = 1;
-        }
-      }
+      mma_kq<NMAX, false>(tmem + Ly::cD1, tmem + Ly::cA1, ptx::smem_u32(B1));
       ptx::mma_commit(mma_bar);
     }
     // arrival: this CTA has finished reading the old q/k window of the key
@@ -751,12 +794,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       float dv[NC];
 #pragma unroll
       for (int c = 0; c < NC / 16; ++c) {
-        float t16[16];
+        float t16[16], u16[16];
         ptx::tmem_ld16(tq + Ly::cD1 + 16 * c, t16);
+        ptx::tmem_ld16(tq + Ly::cD1 + NC + 16 * c, u16);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dv[16 * c + e] = t16[e];
+        for (int e = 0; e < 16; ++e) dv[16 * c + e] = t16[e] + u16[e];
       }
-      ptx::tmem_wait_ld();
       // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
       float rhs[KP];
 #pragma unroll
@@ -845,16 +889,16 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       // read N-major, three passes over K = KP
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kTcD);
-      const uint32_t bhi_a = ptx::smem_u32(Bhi), blo_a = ptx::smem_u32(Blo);
+      const uint32_t b1_a = ptx::smem_u32(B1);
       uint32_t accum = 0;
 #pragma unroll 1
       for (int pass = 0; pass < 3; ++pass) {
         const uint32_t a_col = Ly::cA2 + (pass == 2 ? KH : 0);
-        const uint32_t b_base = pass == 1 ? blo_a : bhi_a;
+        const uint32_t b_base = b1_a + (pass == 1 ? (uint32_t)NC * 128u : 0u);  // lo rows
 #pragma unroll
         for (int ks = 0; ks < KP / 16; ++ks) {
           ptx::mma_bf16_ts(tmem + Ly::cA1, tmem + a_col + 8 * ks,
-                           ptx::sdesc(b_base + 2048u * ks, (uint32_t)NC * 128u, 1024u, 2u), idesc,
+                           ptx::sdesc(b_base + 2048u * ks, (uint32_t)R1 * 128u, 1024u, 2u), idesc,
                            accum);
           accum = 1;
         }
@@ -873,20 +917,31 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::tc_fence_after();
     {
       const float gacc = gam[P - 1] * an[P - 1];
-      float4 *srow = reinterpret_cast<float4 *>(
-          A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD);
+      float *srow =
+          A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float d32[32];
-        ptx::tmem_ld32(tq + Ly::cA1 + 32 * c4, d32);
-        ptx::tmem_wait_ld();
+      for (int c64 = 0; c64 < 2; ++c64) {
+        float d[64];
+        {
+          float d0[32], d1[32];
+          ptx::tmem_ld32(tq + Ly::cA1 + 64 * c64, d0);
+          ptx::tmem_ld32(tq + Ly::cA1 + 64 * c64 + 32, d1);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            d[e] = d0[e];
+            d[32 + e] = d1[e];
+          }
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 s4 =
-              *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, 32 * c4 + 4 * q));
-          srow[8 * c4 + q] = make_float4(fmaf(gacc, s4.x, d32[4 * q]), fmaf(gacc, s4.y, d32[4 * q + 1]),
-                                         fmaf(gacc, s4.z, d32[4 * q + 2]),
-                                         fmaf(gacc, s4.w, d32[4 * q + 3]));
+          const int k = 64 * c64 + 8 * q;
+          const float4 a4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k));
+          const float4 b4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k + 4));
+          stg_v8(srow + k, fmaf(gacc, a4.x, d[8 * q]), fmaf(gacc, a4.y, d[8 * q + 1]),
+                 fmaf(gacc, a4.z, d[8 * q + 2]), fmaf(gacc, a4.w, d[8 * q + 3]),
+                 fmaf(gacc, b4.x, d[8 * q + 4]), fmaf(gacc, b4.y, d[8 * q + 5]),
+                 fmaf(gacc, b4.z, d[8 * q + 6]), fmaf(gacc, b4.w, d[8 * q + 7]));
         }
       }
     }
