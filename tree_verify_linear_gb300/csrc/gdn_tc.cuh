@@ -78,6 +78,7 @@ struct TcLayout {
   static constexpr int kB = R1 * kTcD * 2;            // [K|Q] hi and lo (bf16, 128-byte swizzle)
   static constexpr int kB2 = NC * KP * 2;             // one of [T|W] hi / lo (bf16, no swizzle)
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
+  static constexpr int kNLane = NMAX * (NMAX + 1) / 2;  // (node, ancestor-or-self) pairs
   static constexpr int TP = (NMAX + 3) & ~3;          // row pitch of the fp32 T scratch
   // TMEM columns: S0 hi | lo; the two halves of [S0 k | S0 q] (hi-row and
   // lo-row products); rhs or path deltas (hi | lo).  [delta | W rhs] reuses
@@ -94,7 +95,9 @@ struct TcLayout {
   static constexpr int pj = stg + CS::bytes;          // uint8 [kNPair] parent-path nodes
   static constexpr int gkk = pj + round_up(kNPair, 16);  // float [kNPair] k_j . k_n
   static constexpr int gkq = gkk + 4 * kNPair;        // float [kNPair] k_j . q_n
-  static constexpr int porig = round_up(gkq + 4 * kNPair, 16);  // int [NMAX] parents, input labels
+  static constexpr int pn = gkq + 4 * kNPair;         // uint8 [kNPair] node of each parent-path pair
+  static constexpr int ln = pn + round_up(kNPair, 16);  // uint8 [kNLane] node of each T/W lane
+  static constexpr int porig = round_up(ln + kNLane, 16);  // int [NMAX] parents, input labels
   static constexpr int par = porig + 4 * NMAX;        // int [NMAX] parents, new labels
   static constexpr int dep = par + 4 * NMAX;
   static constexpr int off = dep + 4 * NMAX;          // [NMAX + 4] parent-path offsets
@@ -304,6 +307,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   unsigned char *B2lo = smem + Ly::b2lo;
   float *Tf = reinterpret_cast<float *>(smem + Ly::tf);
   unsigned char *pj = smem + Ly::pj;
+  unsigned char *pn = smem + Ly::pn;
+  unsigned char *ln = smem + Ly::ln;
   float *gkk = reinterpret_cast<float *>(smem + Ly::gkk);
   float *gkq = reinterpret_cast<float *>(smem + Ly::gkq);
   int *porig = reinterpret_cast<int *>(smem + Ly::porig);
@@ -387,11 +392,23 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     x.h = x.kh * G + x.hg;
     return x;
   };
+  // cache slot of a request, read from global memory once per request
+  struct SlotCache {
+    int bq = -1, slot = 0;
+  };
+  auto slot_of = [&](SlotCache &c, int b) {
+    if (b != c.bq) {
+      c.bq = b;
+      c.slot = A.slot[b];
+    }
+    return c.slot;
+  };
+  SlotCache lead_slots, tile_slots;
   // lead thread: copies into the stage and the staging buffer
   int n_state_loads = 0, n_stg_loads = 0;
   auto load_state = [&](int t) {
     const Tile x = tile_of(t);
-    const int srow = ((x.l * A.n_slots + A.slot[x.bq]) * Hv + x.h) * kTcD;
+    const int srow = ((x.l * A.n_slots + slot_of(lead_slots, x.bq)) * Hv + x.h) * kTcD;
     ptx::mbar_arrive_expect_tx(stage_bar, kStageBytes);
     for (int a = 0; a < 4; ++a)
       ptx::tma_load_2d(st + a * (kStageBytes / 4), &maps.state, a * 32, srow, stage_bar);
@@ -402,7 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     const Tile x = tile_of(t);
     const int ch0 = which == 0 ? x.kh * kTcD
                                : (which == 1 ? (Hk + x.kh) * kTcD : (2 * Hk + x.h) * kTcD);
-    const int crow0 = (x.l * A.n_slots + A.slot[x.bq]) * (K - 1);
+    const int crow0 = (x.l * A.n_slots + slot_of(lead_slots, x.bq)) * (K - 1);
     ptx::mbar_arrive_expect_tx(stg_bar, stg_bytes);
     ptx::tma_load_2d(sg + CS::x, &maps.x, ch0, x.lbi * N, stg_bar);
     if (K > 1) ptx::tma_load_2d(sg + CS::c, &maps.cache, ch0, crow0, stg_bar);
@@ -442,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     const Tile x = tile_of(t);
     const int kh = x.kh, bq = x.bq, l = x.l, h = x.h;
     const size_t lb = (size_t)x.lbi;
-    const int slot_b = A.slot[bq];
+    const int slot_b = slot_of(tile_slots, bq);
     float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
 
     // ================= request prologue: tree tables =================
@@ -519,8 +536,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         int j = par[i];
         for (int e = off[i]; e < off[i + 1]; ++e) {
           pj[e] = (unsigned char)j;
+          pn[e] = (unsigned char)i;
           j = par[j];
         }
+        for (int q = off2[i]; q < off2[i + 1]; ++q) ln[q] = (unsigned char)i;
       }
       if (tid == 0) misc[5] = off2[N];
       ptx::named_sync(1, kTcThreads);
@@ -617,8 +636,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         const int npair = off[N];
         for (int item = tid; item < npair + N; item += kTcThreads) {
           if (item < npair) {
-            int n = 0;
-            while (off[n + 1] <= item) ++n;
+            const int n = pn[item];
             const int j = pj[item];
             gkk[item] = Gm[j * NC + n];
             gkq[item] = Gm[j * NC + NMAX + n];
@@ -651,8 +669,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       // stretch m -> n of the parent path (positions 0..L), then W[n][m]
       const int nl = misc[5];
       for (int lane_id = tid; lane_id < nl; lane_id += kTcThreads) {
-        int n = 0;
-        while (off2[n + 1] <= lane_id) ++n;
+        const int n = ln[lane_id];
         const int L = lane_id - off2[n];
         const int e0 = off[n];
         const int m = L == 0 ? n : pj[e0 + L - 1];
