@@ -89,11 +89,16 @@ typedef struct lbx_cfg {
 /* Human-readable text for a status code (static storage). */
 const char *lbx_strerror(int status);
 
-/* Bytes of workspace lbx_verify_step needs for cfg (0 on a bad cfg).  The
- * workspace holds one arrival counter per (layer, request, key head); it must
- * be zero-filled once before its first use, and every call that runs to
- * completion leaves it zero again.  Two calls that run at the same time must
- * not share a workspace. */
+/* Bytes of workspace lbx_verify_step needs for cfg (0 on a bad cfg).  It
+ * must be zero-filled once before its first use; two calls that run at the
+ * same time must not share a workspace.  What it holds depends on the kernel
+ * the configuration selects:
+ *   - the tensor-core step (tree mode, d = 128, N <= 24): the per-request
+ *     tree tables and per-(layer, request, key head) records (q/k operand and
+ *     Gram entries, about 27 KB each at N <= 24) that its prep kernel writes
+ *     and its step kernel reads, rewritten by every call;
+ *   - the CUDA-core kernels: one arrival counter per (layer, request, key
+ *     head); every call that runs to completion leaves them zero again. */
 size_t lbx_workspace_size(const lbx_cfg *cfg);
 
 /*
@@ -168,7 +173,8 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
                     float *o, void *workspace, size_t workspace_bytes, int32_t *d_status,
                     cudaStream_t stream);
 
-/* Capacity of lbx_verify_step_noalloc: L * Bq * Hk <= LBX_NOALLOC_MAX_GROUPS. */
+/* Capacity of lbx_verify_step_noalloc: L * Bq * Hk <= LBX_NOALLOC_MAX_GROUPS
+ * arrival counters (256 KB). */
 #define LBX_NOALLOC_MAX_GROUPS 65536
 
 /*
@@ -182,7 +188,10 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
  * The arrival counters live in a fixed device array inside the library
  * (LBX_NOALLOC_MAX_GROUPS counters, 256 KB), which every GPU that loads the
  * library keeps until the process exits.  Configurations with
- * L * Bq * Hk > LBX_NOALLOC_MAX_GROUPS are rejected with LBX_EINVAL.
+ * L * Bq * Hk > LBX_NOALLOC_MAX_GROUPS are rejected with LBX_EINVAL.  Where
+ * lbx_verify_step would run the tensor-core step, whose workspace is larger
+ * than the array, this function runs the CUDA-core tree kernel instead
+ * (results agree within the tolerances of the tests; only speed differs).
  * The function allocates nothing: no cudaMalloc, cudaFree or other
  * allocating call.
  *   - The first call on each device looks up the array's device address

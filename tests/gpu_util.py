@@ -41,6 +41,21 @@ def run_verify(w, inp, mode=lbx.LBX_MODE_AUTO, steps=1, ws=None):
             int(status.item()), ws.cpu().numpy())
 
 
+def uses_tensor_cores(w, mode=lbx.LBX_MODE_AUTO) -> bool:
+    """Whether lbx_verify_step runs the tensor-core step (tree mode, d = 128,
+    N <= 24), whose workspace holds the prep kernel's records instead of
+    arrival counters."""
+    if mode == lbx.LBX_MODE_AUTO:
+        mode = lbx.LBX_MODE_TREE if w.N <= lbx.LBX_MAX_TREE_NODES else lbx.LBX_MODE_CHUNKED
+    return mode == lbx.LBX_MODE_TREE and w.d == 128 and w.N <= 24
+
+
+def counters_cleared(w, ws: np.ndarray, mode=lbx.LBX_MODE_AUTO) -> bool:
+    """The CUDA-core kernels leave their arrival counters at zero; the
+    tensor-core step's workspace holds records and is not checked."""
+    return uses_tensor_cores(w, mode) or not ws.any()
+
+
 def o_error(o_gpu: np.ndarray, o_ref: np.ndarray) -> float:
     """max |o_gpu - o_ref| / max |o_ref|."""
     return float(np.abs(o_gpu.astype(np.float64) - o_ref).max() / np.abs(o_ref).max())

@@ -37,9 +37,16 @@ int launch_step_fused(const StepArgs &A, int d, cudaStream_t st);
 // Recurrence from a conv output; node_states written when A.node_states != NULL.
 int launch_step_unfused(const StepArgs &A, int d, cudaStream_t st);
 
-// Tensor-core fused step (d = 128, tree mode, N <= 24).
+// Tensor-core fused step (d = 128, tree mode, N <= 24): a prep kernel per key
+// head, then the step kernel.  Its workspace holds the prep kernel's tables
+// and records (step_tc_workspace_bytes); no arrival counters.
 bool step_tc_supported(int d, int N, int chain);
-int launch_step_tc(const StepArgs &A, cudaStream_t st);
+size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int N);
+int launch_step_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st);
+
+// Workspace of the CUDA-core fused step: one arrival counter per (layer,
+// request, key head), 256-byte rounded.
+size_t counters_bytes(int L, int Bq, int Hk);
 
 // Row-block size and product-tile width used for head dimension d and node
 // capacity cap; returns the dynamic shared memory bytes (0 if unsupported).

@@ -1,5 +1,6 @@
 // gdn_step_tc.cu -- host launch of the tensor-core fused step (d = 128, tree
 // mode, N <= 24): tensor maps of the state, the raw inputs and the conv cache;
+// the prep kernel (one CTA per key head), then the step kernel on a
 // persistent grid of two CTAs per SM.
 #include <cudaTypedefs.h>
 
@@ -8,6 +9,7 @@
 
 #include "gdn_launch.h"
 #include "gdn_tc.cuh"
+#include "gdn_tc_prep.cuh"
 
 namespace lbx {
 namespace {
@@ -53,7 +55,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *
 }
 
 template <int NMAX>
-int launch_tc(const StepArgs &A, cudaStream_t st) {
+int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
+  if (ws == nullptr || ws_bytes < tc_workspace_bytes<NMAX>(A.L, A.Bq, A.Hk)) return LBX_EINVAL;
+  if (((uintptr_t)ws & 15u) != 0) return LBX_EINVAL;
   if (!have_encode()) return LBX_ECUDA;
   const int nsm = sm_count();
   if (nsm <= 0) return LBX_ECUDA;
@@ -77,6 +81,16 @@ int launch_tc(const StepArgs &A, cudaStream_t st) {
   TcArgs T;
   T.s = A;
   T.n_tiles = A.L * A.Bq * A.Hv;
+  T.ws = static_cast<unsigned char *>(ws);
+  {
+    auto prep = gdn_qk_prep_kernel<NMAX>;
+    constexpr int psmem = PrepLayout<NMAX>::total;
+    if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem) !=
+        cudaSuccess)
+      return LBX_ECUDA;
+    prep<<<A.L * A.Bq * A.Hk, kPrepThreads, psmem, st>>>(maps, T);
+    if (cudaGetLastError() != cudaSuccess) return LBX_ECUDA;
+  }
   auto kern = gdn_step_tc_kernel<NMAX>;
   constexpr int smem = TcLayout<NMAX>::smem_bytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -96,12 +110,19 @@ bool step_tc_supported(int d, int N, int chain) {
   return d == kTcD && !chain && N >= 1 && N <= 24;
 }
 
-int launch_step_tc(const StepArgs &A, cudaStream_t st) {
+size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int N) {
+  if (N <= 8) return tc_workspace_bytes<8>(L, Bq, Hk);
+  if (N <= 16) return tc_workspace_bytes<16>(L, Bq, Hk);
+  if (N <= 24) return tc_workspace_bytes<24>(L, Bq, Hk);
+  return 0;
+}
+
+int launch_step_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
   if ((long long)A.L * A.n_slots * A.Hv * kTcD > 0x7fffffffLL) return LBX_EINVAL;
   if ((long long)A.L * A.Bq * A.N > 0x7fffffffLL) return LBX_EINVAL;
-  if (A.N <= 8) return launch_tc<8>(A, st);
-  if (A.N <= 16) return launch_tc<16>(A, st);
-  if (A.N <= 24) return launch_tc<24>(A, st);
+  if (A.N <= 8) return launch_tc<8>(A, ws, ws_bytes, st);
+  if (A.N <= 16) return launch_tc<16>(A, ws, ws_bytes, st);
+  if (A.N <= 24) return launch_tc<24>(A, ws, ws_bytes, st);
   return LBX_EINVAL;
 }
 

@@ -2,20 +2,23 @@
 //
 // Two CTAs share each SM (at most 113 KB of shared memory and 256 TMEM
 // columns each), so the latency-bound phases of one CTA overlap the other's.
-// A CTA has 4 warps, thread = state row = TMEM lane.  The work is a list of
-// tiles, one per (layer l, request b, value head h) = one 128 x 128 fp32 state
-// slab, ordered (l, b, key head, head in group); every CTA takes a contiguous
-// range, so consecutive tiles usually share their request and key head: the
-// tree tables are built once per request and the q/k prologue once per key
-// head.
+// A CTA has 8 warps; warps w and w + 4 share TMEM lane quadrant w, and each
+// state row (= TMEM lane) has two threads, one per half: of the 128 columns
+// when the state is split and written back, of the nodes in the row work.
+// The work is a list of tiles, one per (layer l, request b, value head h) =
+// one 128 x 128 fp32 state slab, ordered (l, b, key head, head in group);
+// every CTA takes a contiguous range, so consecutive tiles usually share
+// their request and key head.  The prep kernel (gdn_tc_prep.cuh) has already
+// built, per request, the tree tables and, per key head, the [K|Q] operand
+// and the Gram entries; the step kernel bulk-copies them from the workspace
+// when the request or the key head changes.
 //
 // Nodes are relabelled per request so that the accepted path comes first
 // (root = 0, ..., accepted node = P-1) and the rest follow in index order;
-// parents still precede children.  Global inputs arrive by bulk-async copies
-// issued by thread 0: the state slab S0 (TMA, four 32-column boxes, 128-byte
-// swizzle) into the stage, and the raw inputs, cached window rows and conv
-// weights of one 128-channel block at a time into the staging buffer (q then
-// k when a key head starts, then the value head's channels).
+// parents still precede children.  Thread 0 also issues the bulk-async copies
+// of the state slab S0 (TMA, four 32-column boxes, 128-byte swizzle) into the
+// stage and of the raw inputs, cached window rows and conv weights of the
+// value head's 128 channels into the staging buffer, one tile ahead.
 //
 // With the factored delta rule S_n = gamma_n S0 + sum_{j in path(n)}
 // g(j->n) delta_j k_j^T (g = product of the gates strictly after j), every
@@ -28,7 +31,7 @@
 //   MMA1  [S0 k_n | S0 q_n]      = S0 [K | Q]^T      (A = S0 in TMEM, K = 128)
 //   MMA2  [delta_n | (W rhs)_n]  = rhs [T | W]^T     (A = rhs in TMEM, K = N)
 //   MMA3  sum_j c_j delta_j k_j^T = (c . delta) K     (A = path deltas, K = P,
-//         B = the first rows of operand K read N-major)
+//         B = the K rows of the operand read N-major)
 // and the accepted state gamma_acc S0 + MMA3 is written straight to global
 // memory.  T and W (shared by the 128 rows) are built by one lane per
 // (node, ancestor-or-self) pair, each walking its stretch of the parent path,
@@ -36,12 +39,13 @@
 // and run without run-time guards: padding nodes carry zero gates, taps
 // beyond the conv width zero weights, every load a clamped, valid index.
 // The conv window of the slot is persisted in place: every value channel by
-// its row thread, and the q/k channels by the CTA whose tile is the last of
-// its key-head group to arrive (arrival counter).
+// its row thread here, the q/k channels by the prep kernel.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "gdn_common.cuh"
 #include "gdn_step.cuh"
@@ -50,7 +54,7 @@
 namespace lbx {
 
 constexpr int kTcD = 128;                      // head dimension of this kernel
-constexpr int kTcThreads = 128;                // 4 warps, thread = state row
+constexpr int kTcThreads = 256;                // 8 warps, two threads per state row
 constexpr int kTcCtasPerSm = 2;
 constexpr uint32_t kTcTmemCols = 256;          // per CTA: two CTAs fill the 512 columns
 constexpr uint32_t kStageBytes = kTcD * kTcD * 4;  // one state slab, 64 KB
@@ -69,6 +73,45 @@ struct ConvStage {
   static constexpr int bytes = round_up(w + kTcD * LBX_MAX_CONV_WIDTH * 2, 128);
 };
 
+// Per-request tree tables in the new labels (built by the prep kernel, one
+// bulk copy into the step kernel): parent-path nodes pj and their node pn per
+// (node, strict ancestor) pair, node ln per (node, ancestor-or-self) lane,
+// parents, depths, pair and lane offsets, conv window sources (input x row
+// >= 0, or cached row -1-w), label maps, new-window sources and
+// {P = accepted-path length, lanes, pairs}.
+template <int NMAX>
+struct TabLayout {
+  static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
+  static constexpr int kNLane = NMAX * (NMAX + 1) / 2;
+  static constexpr int pj = 0;                          // uint8 [kNPair]
+  static constexpr int pn = pj + round_up(kNPair, 16);  // uint8 [kNPair]
+  static constexpr int ln = pn + round_up(kNPair, 16);  // uint8 [kNLane]
+  static constexpr int par = ln + round_up(kNLane, 16); // int [NMAX]
+  static constexpr int dep = par + 4 * round_up(NMAX, 4);
+  static constexpr int off = dep + 4 * round_up(NMAX, 4);      // [NMAX + 4]
+  static constexpr int off2 = off + 4 * (NMAX + 4);            // [NMAX + 4]
+  static constexpr int win = off2 + 4 * (NMAX + 4);            // [NMAX][4]
+  static constexpr int n2o = win + 16 * NMAX;
+  static constexpr int o2n = n2o + 4 * round_up(NMAX, 4);
+  static constexpr int crow = o2n + 4 * round_up(NMAX, 4);     // [4]
+  static constexpr int meta = crow + 16;                       // [4] P, lanes, pairs
+  static constexpr int bytes = meta + 16;
+  static_assert(win % 16 == 0 && bytes % 16 == 0, "alignment");
+};
+
+// Per-key-head record (built by the prep kernel): the [K|Q] operand image
+// (see TcLayout::b1) followed by the Gram entries k_j.k_n, k_j.q_n of the
+// parent-path pairs and the diagonals k_n.q_n.
+template <int NMAX>
+struct GramLayout {
+  static constexpr int kNPairP = round_up(NMAX * (NMAX - 1) / 2 + 1, 4);
+  static constexpr int gkk = 0;
+  static constexpr int gkq = gkk + 4 * kNPairP;
+  static constexpr int kqn = gkq + 4 * kNPairP;
+  static constexpr int bytes = kqn + 4 * round_up(NMAX, 4);
+  static_assert(bytes % 16 == 0, "alignment");
+};
+
 template <int NMAX>
 struct TcLayout {
   using CS = ConvStage<NMAX>;
@@ -77,58 +120,69 @@ struct TcLayout {
   static constexpr int KP = round_up(NMAX, 16);       // node dimension padded to the MMA K step
   static constexpr int kB = R1 * kTcD * 2;            // [K|Q] hi and lo (bf16, 128-byte swizzle)
   static constexpr int kB2 = NC * KP * 2;             // one of [T|W] hi / lo (bf16, no swizzle)
-  static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
-  static constexpr int kNLane = NMAX * (NMAX + 1) / 2;  // (node, ancestor-or-self) pairs
   static constexpr int TP = (NMAX + 3) & ~3;          // row pitch of the fp32 T scratch
   // TMEM columns: S0 hi | lo; the two halves of [S0 k | S0 q] (hi-row and
   // lo-row products); rhs or path deltas (hi | lo).  [delta | W rhs] reuses
-  // the first half of the MMA1 accumulator, the Gram product and the MMA3
-  // accumulator the S0 columns.
+  // the first half of the MMA1 accumulator, the MMA3 accumulator the S0
+  // columns.
   static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + R1, cD2 = cD1;
   static_assert(cA2 + KP <= kTcTmemCols, "tensor memory");
+  // per-key-head record in the workspace: [K|Q] image, then Gram entries
+  static constexpr int rec_bytes = kB + GramLayout<NMAX>::bytes;
   static constexpr int stage = 0;
-  static constexpr int b1 = stage + (int)kStageBytes;
-  static constexpr int b2hi = b1 + kB;
+  static constexpr int b1 = stage + (int)kStageBytes;  // record: [K|Q] image ...
+  static constexpr int gr = b1 + kB;                   // ... and Gram entries
+  static constexpr int b2hi = gr + GramLayout<NMAX>::bytes;
   static constexpr int b2lo = b2hi + kB2;
   static constexpr int tf = b2lo + kB2;               // float [NMAX][TP] T scratch
-  static constexpr int stg = round_up(tf + NMAX * TP * 4, 128);  // conv-input staging
-  static constexpr int pj = stg + CS::bytes;          // uint8 [kNPair] parent-path nodes
-  static constexpr int gkk = pj + round_up(kNPair, 16);  // float [kNPair] k_j . k_n
-  static constexpr int gkq = gkk + 4 * kNPair;        // float [kNPair] k_j . q_n
-  static constexpr int pn = gkq + 4 * kNPair;         // uint8 [kNPair] node of each parent-path pair
-  static constexpr int ln = pn + round_up(kNPair, 16);  // uint8 [kNLane] node of each T/W lane
-  static constexpr int porig = round_up(ln + kNLane, 16);  // int [NMAX] parents, input labels
-  static constexpr int par = porig + 4 * NMAX;        // int [NMAX] parents, new labels
-  static constexpr int dep = par + 4 * NMAX;
-  static constexpr int off = dep + 4 * NMAX;          // [NMAX + 4] parent-path offsets
-  static constexpr int off2 = off + 4 * (NMAX + 4);   // [NMAX + 4] T/W lane offsets
-  static constexpr int win = off2 + 4 * (NMAX + 4);   // [NMAX][4] conv window sources (16-byte rows)
-  static constexpr int n2o = win + 16 * NMAX;         // new label -> input label
-  static constexpr int o2n = n2o + 4 * NMAX;          // input label -> new label
-  static constexpr int an = o2n + 4 * NMAX;
+  static constexpr int stg = round_up(tf + NMAX * TP * 4, 128);  // value-head conv inputs
+  static constexpr int tb = stg + CS::bytes;          // tree tables
+  static constexpr int an = tb + TabLayout<NMAX>::bytes;
   static constexpr int bn = an + 4 * NMAX;
   static constexpr int gam = bn + 4 * NMAX;           // gamma of the parent
   static constexpr int cpa = gam + 4 * NMAX;          // path coefficients g(j->acc)
-  static constexpr int kqn = cpa + 4 * NMAX;
-  static constexpr int crow = kqn + 4 * NMAX;         // [4] new-window sources
-  static constexpr int misc = crow + 16;              // ints, see kernel
-  static constexpr int bars = (misc + 64 + 7) & ~7;   // 3 x uint64
-  static constexpr int total = bars + 3 * 8;
-  // The Gram product reads A = 128 rows of the [K|Q] operand per K step
-  // (rows past the K rows feed accumulator lanes that are not used): the
-  // last byte it can touch is 16 KB past the start of the second 64-column
-  // atom of the lo rows.  The allocation covers that range.
-  static constexpr int gram_extent = b1 + NC * 128 + R1 * 128 + 128 * 128;
-  static constexpr int smem_bytes = total > gram_extent ? total : gram_extent;
+  static constexpr int misc = cpa + 4 * NMAX;         // ints, see kernel
+  static constexpr int bars = (misc + 64 + 7) & ~7;   // 5 x uint64
+  static constexpr int total = bars + 5 * 8;
+  static constexpr int smem_bytes = total;
   static_assert(kB % 1024 == 0, "operand [K|Q] must keep 1024-byte alignment");
   static_assert(smem_bytes <= kTcMaxSmem, "two CTAs per SM");
-  static_assert(win % 16 == 0 && stg % 128 == 0 && b2hi % 16 == 0, "alignment");
-  static_assert(NMAX * NC * 4 <= 2 * kB2, "the Gram matrix is staged in the [T|W] buffer");
+  static_assert(stg % 128 == 0 && tb % 16 == 0 && b2hi % 16 == 0 && gr % 16 == 0, "alignment");
 };
+
+// Shared memory of the prep kernel (one CTA per key head).
+template <int NMAX>
+struct PrepLayout {
+  using Ly = TcLayout<NMAX>;
+  using CS = ConvStage<NMAX>;
+  static constexpr int b1 = 0;                        // [K|Q] image
+  static constexpr int kqf = b1 + Ly::kB;             // fp32 [NC][128]: k rows, then q rows
+  static constexpr int sq = kqf + Ly::NC * kTcD * 4;  // staged q inputs
+  static constexpr int sk = sq + CS::bytes;           // staged k inputs
+  static constexpr int gr = sk + CS::bytes;           // Gram entries
+  static constexpr int tb = gr + GramLayout<NMAX>::bytes;
+  static constexpr int porig = tb + TabLayout<NMAX>::bytes;  // int [NMAX] input parents
+  static constexpr int misc = porig + 4 * round_up(NMAX, 4);
+  static constexpr int bar = (misc + 64 + 7) & ~7;
+  static constexpr int total = bar + 8;
+  static_assert(sq % 128 == 0 && sk % 128 == 0, "TMA destinations");
+};
+
+// Workspace layout of the tensor-core step: the tree tables of every request,
+// then one record per (layer, request, key head).
+template <int NMAX>
+__host__ __device__ inline size_t tc_tab_bytes(int Bq) {
+  return ((size_t)Bq * TabLayout<NMAX>::bytes + 255) & ~(size_t)255;
+}
+template <int NMAX>
+__host__ __device__ inline size_t tc_workspace_bytes(int L, int Bq, int Hk) {
+  return tc_tab_bytes<NMAX>(Bq) + (size_t)L * Bq * Hk * TcLayout<NMAX>::rec_bytes;
+}
 
 struct TcArgs {
   StepArgs s;
-  int n_tiles;  // L * Bq * Hv
+  int n_tiles;        // L * Bq * Hv
+  unsigned char *ws;  // workspace: tree tables, then per-key-head records
 };
 
 struct TcMaps {
@@ -264,13 +318,30 @@ __device__ __forceinline__ void persist_channel_global(int gc, int K, int C, con
     if (rr < K - 1) cache_out[(size_t)rr * C + gc] = val[rr];
 }
 
-// Product with B = [K|Q] (hi rows 0..NC-1, lo rows NC..2NC-1, K = 128,
-// 128-byte swizzle) and a bf16 hi / lo operand A over the same K: pass 1,
-// A_hi x [B_hi | B_lo] (N = 2 NC), initialises 2 NC accumulator columns and
-// pass 2, A_lo x B_hi, adds into the first NC; column n of the result is the
-// sum of columns n and NC + n.  A is in TMEM (S0: hi columns a, lo columns
-// a + 64) or, when A_SMEM, the K rows of B itself (hi rows, then lo rows).
-template <int NMAX, bool A_SMEM>
+// Node values of half HF of a row (NMAX / 2 nodes), as packed bf16 pairs,
+// hi and lo, into the A columns of MMA2 / MMA3 (hi at a2, lo at a2 + KP/2):
+// half 0 writes pairs 0 .. C0-1, half 1 pairs C0 .. KP/2-1 (its nodes, then
+// the zero padding up to KP).
+template <int NMAX, int HF>
+__device__ __forceinline__ void store_pairs(uint32_t a2, const float *v) {
+  using Ly = TcLayout<NMAX>;
+  constexpr int NH = NMAX / 2, KP = Ly::KP, KH = KP / 2;
+  constexpr int C0 = NH / 2, C1 = (NH + KP - NMAX) / 2;
+  constexpr int CNT = HF ? C1 : C0, OFF = HF ? C0 : 0;
+  uint32_t ph[CNT], pl[CNT];
+#pragma unroll
+  for (int e = 0; e < CNT; ++e)
+    split_bf16x2(2 * e < NH ? v[2 * e] : 0.f, 2 * e + 1 < NH ? v[2 * e + 1] : 0.f, ph[e], pl[e]);
+  ptx::tmem_st_run<OFF, CNT>(a2, ph);
+  ptx::tmem_st_run<OFF, CNT>(a2 + KH, pl);
+}
+
+// MMA1: S0 [K|Q]^T with B = [K|Q] (hi rows 0..NC-1, lo rows NC..2NC-1,
+// K = 128, 128-byte swizzle) and S0 in TMEM (hi columns a, lo columns
+// a + 64): pass 1, S0_hi x [B_hi | B_lo] (N = 2 NC), initialises 2 NC
+// accumulator columns and pass 2, S0_lo x B_hi, adds into the first NC;
+// column n of the product is the sum of columns n and NC + n.
+template <int NMAX>
 __device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t a, uint32_t b1) {
   using Ly = TcLayout<NMAX>;
   constexpr int NC = Ly::NC, R1 = Ly::R1;
@@ -280,14 +351,8 @@ __device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t a, uint32_t b1)
 #pragma unroll
     for (int ks = 0; ks < kTcD / 16; ++ks) {
       const uint32_t koff = (uint32_t)((ks >> 2) * (R1 * 128) + (ks & 3) * 32);
-      const uint64_t bdesc = ptx::sdesc_sw128(b1 + koff);
-      const uint32_t acc = (pass | ks) != 0;
-      if constexpr (A_SMEM) {
-        const uint32_t abase = a + (pass == 1 ? (uint32_t)NC * 128u : 0u);
-        ptx::mma_bf16_ss(d_tmem, ptx::sdesc_sw128(abase + koff), bdesc, idesc, acc);
-      } else {
-        ptx::mma_bf16_ts(d_tmem, a + (pass == 1 ? 64u : 0u) + 8u * ks, bdesc, idesc, acc);
-      }
+      ptx::mma_bf16_ts(d_tmem, a + (pass == 1 ? 64u : 0u) + 8u * ks, ptx::sdesc_sw128(b1 + koff),
+                       idesc, (pass | ks) != 0);
     }
   }
 }
@@ -305,32 +370,34 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   unsigned char *B1 = smem + Ly::b1;  // [K|Q] hi rows 0..NC-1, lo rows NC..2NC-1
   unsigned char *B2hi = smem + Ly::b2hi;
   unsigned char *B2lo = smem + Ly::b2lo;
+  using TL = TabLayout<NMAX>;
+  using GL = GramLayout<NMAX>;
   float *Tf = reinterpret_cast<float *>(smem + Ly::tf);
-  unsigned char *pj = smem + Ly::pj;
-  unsigned char *pn = smem + Ly::pn;
-  unsigned char *ln = smem + Ly::ln;
-  float *gkk = reinterpret_cast<float *>(smem + Ly::gkk);
-  float *gkq = reinterpret_cast<float *>(smem + Ly::gkq);
-  int *porig = reinterpret_cast<int *>(smem + Ly::porig);
-  int *par = reinterpret_cast<int *>(smem + Ly::par);
-  int *dep = reinterpret_cast<int *>(smem + Ly::dep);
-  int *off = reinterpret_cast<int *>(smem + Ly::off);
-  int *off2 = reinterpret_cast<int *>(smem + Ly::off2);
-  int *win = reinterpret_cast<int *>(smem + Ly::win);
-  int *n2o = reinterpret_cast<int *>(smem + Ly::n2o);
-  int *o2n = reinterpret_cast<int *>(smem + Ly::o2n);
+  unsigned char *tb = smem + Ly::tb;
+  const unsigned char *pj = tb + TL::pj;
+  const unsigned char *ln = tb + TL::ln;
+  const int *dep = reinterpret_cast<const int *>(tb + TL::dep);
+  const int *off = reinterpret_cast<const int *>(tb + TL::off);
+  const int *off2 = reinterpret_cast<const int *>(tb + TL::off2);
+  const int *win = reinterpret_cast<const int *>(tb + TL::win);
+  const int *n2o = reinterpret_cast<const int *>(tb + TL::n2o);
+  const int *o2n = reinterpret_cast<const int *>(tb + TL::o2n);
+  const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
+  const int *meta = reinterpret_cast<const int *>(tb + TL::meta);  // P, lanes, pairs
+  const float *gkk = reinterpret_cast<const float *>(smem + Ly::gr + GL::gkk);
+  const float *gkq = reinterpret_cast<const float *>(smem + Ly::gr + GL::gkq);
+  const float *kqn = reinterpret_cast<const float *>(smem + Ly::gr + GL::kqn);
   float *an = reinterpret_cast<float *>(smem + Ly::an);
   float *bn = reinterpret_cast<float *>(smem + Ly::bn);
   float *gam = reinterpret_cast<float *>(smem + Ly::gam);
   float *cpa = reinterpret_cast<float *>(smem + Ly::cpa);
-  float *kqn = reinterpret_cast<float *>(smem + Ly::kqn);
-  int *crow = reinterpret_cast<int *>(smem + Ly::crow);
   int *misc = reinterpret_cast<int *>(smem + Ly::misc);
-  // misc[0] error flag, [1] abort, [2] last arriver, [3] TMEM base,
-  // [4] accepted-path length P, [5] number of T/W lanes
+  // misc[0] error flag, [1] abort, [3] TMEM base
   uint64_t *stage_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);
   uint64_t *stg_bar = stage_bar + 1;
   uint64_t *mma_bar = stage_bar + 2;
+  uint64_t *rec_bar = stage_bar + 3;  // per-key-head record
+  uint64_t *tab_bar = stage_bar + 4;  // per-request tables
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -365,6 +432,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::mbar_init(stage_bar, 1);
     ptx::mbar_init(stg_bar, 1);
     ptx::mbar_init(mma_bar, 1);
+    ptx::mbar_init(rec_bar, 1);
+    ptx::mbar_init(tab_bar, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -414,11 +483,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       ptx::tma_load_2d(st + a * (kStageBytes / 4), &maps.state, a * 32, srow, stage_bar);
     ++n_state_loads;
   };
-  // which: 0 = q, 1 = k, 2 = the value head's channels
-  auto load_block = [&](int t, int which) {
+  // conv inputs of the value head's channels
+  auto load_block = [&](int t) {
     const Tile x = tile_of(t);
-    const int ch0 = which == 0 ? x.kh * kTcD
-                               : (which == 1 ? (Hk + x.kh) * kTcD : (2 * Hk + x.h) * kTcD);
+    const int ch0 = (2 * Hk + x.h) * kTcD;
     const int crow0 = (x.l * A.n_slots + slot_of(lead_slots, x.bq)) * (K - 1);
     ptx::mbar_arrive_expect_tx(stg_bar, stg_bytes);
     ptx::tma_load_2d(sg + CS::x, &maps.x, ch0, x.lbi * N, stg_bar);
@@ -427,8 +495,26 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
                    (uint32_t)kTcD * K * 2, stg_bar);
     ++n_stg_loads;
   };
+  // the key head's record ([K|Q] image and Gram entries) and the request's
+  // tree tables, from the workspace the prep kernel filled
+  int n_rec_loads = 0, n_tab_loads = 0;
+  const unsigned char *recs = T.ws + tc_tab_bytes<NMAX>(Bq);
+  auto load_rec = [&](int t) {
+    const Tile x = tile_of(t);
+    const unsigned char *src = recs + (size_t)x.rest * Ly::rec_bytes;
+    ptx::mbar_arrive_expect_tx(rec_bar, (uint32_t)Ly::rec_bytes);
+    ptx::bulk_load(B1, src, (uint32_t)Ly::kB, rec_bar);
+    ptx::bulk_load(smem + Ly::gr, src + Ly::kB, (uint32_t)GL::bytes, rec_bar);
+    ++n_rec_loads;
+  };
+  auto load_tab = [&](int t) {
+    const Tile x = tile_of(t);
+    ptx::mbar_arrive_expect_tx(tab_bar, (uint32_t)TL::bytes);
+    ptx::bulk_load(tb, T.ws + (size_t)x.bq * TL::bytes, (uint32_t)TL::bytes, tab_bar);
+    ++n_tab_loads;
+  };
   // phases waited for, the same count in every thread
-  uint32_t stg_waits = 0, mma_waits = 0;
+  uint32_t stg_waits = 0, mma_waits = 0, rec_waits = 0, tab_waits = 0;
   auto wait_on = [&](uint64_t *bar, uint32_t &waits) {
     if (!ptx::mbar_wait(bar, waits & 1u)) {
       if (A.status) *A.status = LBX_ETIMEOUT;
@@ -438,12 +524,21 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   };
 
   if (lead && count > 0) {
+    load_tab(t_begin);
+    load_rec(t_begin);
     load_state(t_begin);
-    load_block(t_begin, 0);
+    load_block(t_begin);
   }
 
-  const int r = tid;  // state row = TMEM lane
-  const uint32_t tq = tmem + ((uint32_t)(warp * 32) << 16);
+  // state row r (= TMEM lane) and half hf of this thread; the row work of
+  // nodes n0 .. n0 + NH - 1 is this thread's
+  const int quad = warp & 3, hf = warp >> 2;
+  const int r = quad * 32 + (tid & 31);
+  const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+  constexpr int NH = NMAX / 2;                        // nodes per half
+  static_assert(NH % 2 == 0, "node halves");
+  const int n0 = hf * NH;
+  constexpr int LB = NH <= 4 ? 4 : 8;  // accumulator columns per TMEM load
 
   // gates of the current tile for input node tid (< N), prefetched
   float ga = 0.f, gb = 0.f;
@@ -457,198 +552,22 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   for (int it = 0; it < count; ++it) {
     const int t = t_begin + it;
     const Tile x = tile_of(t);
-    const int kh = x.kh, bq = x.bq, l = x.l, h = x.h;
+    const int bq = x.bq, l = x.l, h = x.h;
     const size_t lb = (size_t)x.lbi;
     const int slot_b = slot_of(tile_slots, bq);
     float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
 
-    // ================= request prologue: tree tables =================
+    // ================= tree tables (new request), record (new key head) =================
     if (bq != cur_req) {
       cur_req = bq;
-      const int32_t *par_b = A.parent + (size_t)bq * N;
-      const int acc = A.accepted[bq];
-      if (tid < NMAX) {
-        porig[tid] = tid < N ? par_b[tid] : -1;
-        o2n[tid] = -1;
-      }
       // [T | W] entries outside the (node, ancestor-or-self) pairs stay zero
       for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
         *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
-      ptx::named_sync(1, kTcThreads);
-      if (tid == 0) {
-        // the accepted path, root first, takes labels 0..P-1; the other
-        // nodes follow in input order
-        int P = 0;
-        for (int m = acc; m >= 0; m = porig[m]) ++P;
-        int p = P;
-        for (int m = acc; m >= 0; m = porig[m]) {
-          --p;
-          n2o[p] = m;
-          o2n[m] = p;
-        }
-        int c = P;
-        for (int i = 0; i < N; ++i)
-          if (o2n[i] < 0) {
-            n2o[c] = i;
-            o2n[i] = c;
-            ++c;
-          }
-        misc[4] = P;
-      }
-      if (tid == 32) window_sources(crow, K, acc, porig);
-      ptx::named_sync(1, kTcThreads);
-      if (tid < NMAX) {
-        // parent, depth and conv window rows in the new labels; taps j >= K
-        // and padding nodes point at input row 0
-        const int o = tid < N ? n2o[tid] : 0;
-        par[tid] = tid < N && porig[o] >= 0 ? o2n[porig[o]] : -1;
-        int d = 0;
-        if (tid < N)
-          for (int m = porig[o]; m >= 0; m = porig[m]) ++d;
-        dep[tid] = d;
-        int m = tid < N ? o : -2, past = 0;
-        for (int j = 0; j < 4; ++j) {
-          int w = 0;
-          if (tid < N && j < K) {
-            if (m >= 0) {
-              w = m;
-              m = porig[m];
-            } else {
-              ++past;
-              w = -1 - (K - 1 - past);
-            }
-          }
-          win[tid * 4 + j] = w;
-        }
-      }
-      ptx::named_sync(1, kTcThreads);
-      if (tid <= NMAX) {
-        int o1 = 0, o2 = 0;
-        for (int i = 0; i < N && i < tid; ++i) {
-          o1 += dep[i];
-          o2 += dep[i] + 1;
-        }
-        off[tid] = o1;
-        off2[tid] = o2;
-      }
-      ptx::named_sync(1, kTcThreads);
-      for (int i = tid; i < N; i += kTcThreads) {
-        int j = par[i];
-        for (int e = off[i]; e < off[i + 1]; ++e) {
-          pj[e] = (unsigned char)j;
-          pn[e] = (unsigned char)i;
-          j = par[j];
-        }
-        for (int q = off2[i]; q < off2[i + 1]; ++q) ln[q] = (unsigned char)i;
-      }
-      if (tid == 0) misc[5] = off2[N];
-      ptx::named_sync(1, kTcThreads);
+      wait_on(tab_bar, tab_waits);
     }
-
-    // ================= group prologue (new key head) =================
     if (x.rest != cur_group) {
       cur_group = x.rest;
-      // q, then k: conv + SiLU + L2 from the staged inputs -> operand rows
-      // (bf16 hi / lo); q scaled
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        wait_on(stg_bar, stg_waits);
-        constexpr int GQ = kTcD / 8;  // 16 threads per node, the same 8 channels for every node
-        constexpr int U = (NMAX * GQ + kTcThreads - 1) / kTcThreads;
-        static_assert(kTcThreads % GQ == 0, "channel group fixed per thread");
-        const int units = N * GQ;
-        const int li = tid % GQ;
-        float wsl[8][LBX_MAX_CONV_WIDTH];
-        conv_weights8<NMAX>(wsl, K, sg, li * 8);
-#pragma unroll
-        for (int p = 0; p < U; ++p) {
-          const int u = p * kTcThreads + tid;
-          const bool act = u < units;
-          const int i = act ? u / GQ : 0;
-          float v8[8];
-          conv8_staged<NMAX>(v8, win + i * 4, wsl, sg, li * 8);
-          float ss = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
-#pragma unroll
-          for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-          if (act) {
-            const float scale = rsqrtf(ss + A.l2_eps) * (which == 0 ? A.q_scale : 1.f);
-            const int brow = which == 0 ? NMAX + i : i;
-            uint32_t wh[4], wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              split_bf16x2(scale * v8[2 * e], scale * v8[2 * e + 1], wh[e], wl[e]);
-            *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, li * 8)) =
-                make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, li * 8)) =
-                make_uint4(wl[0], wl[1], wl[2], wl[3]);
-          }
-        }
-        // zero the padding rows of this half of the operand
-        for (int idx = tid; idx < (NMAX - N) * 16; idx += kTcThreads) {
-          const int brow = (which == 0 ? NMAX : 0) + N + idx / 16;
-          *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, 8 * (idx % 16))) =
-              make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, 8 * (idx % 16))) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        ptx::named_sync(1, kTcThreads);  // staging consumed
-        if (lead) load_block(t, which == 0 ? 1 : 2);
-      }
-      // Gram matrix K [K|Q]^T on the tensor cores (A = the K rows of the
-      // operand, read from shared memory; rows >= NMAX of the product are
-      // not used), staged as fp32 [NMAX][NC] in the [T|W] buffer
-      ptx::fence_proxy_async();
-      ptx::tc_fence_before();
-      ptx::named_sync(1, kTcThreads);
-      if (lead) {
-        ptx::tc_fence_after();
-        mma_kq<NMAX, true>(tmem + Ly::cA1, ptx::smem_u32(B1), ptx::smem_u32(B1));
-        ptx::mma_commit(mma_bar);
-      }
-      wait_on(mma_bar, mma_waits);
-      ptx::tc_fence_after();
-      float *Gm = reinterpret_cast<float *>(B2hi);
-      if (warp == 0) {
-        float g[R1];
-#pragma unroll
-        for (int c = 0; c < R1 / 32; ++c) {
-          float t32[32];
-          ptx::tmem_ld32(tq + Ly::cA1 + 32 * c, t32);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) g[32 * c + e] = t32[e];
-        }
-        ptx::tmem_wait_ld();
-        if (tid < NMAX) {
-#pragma unroll
-          for (int n4 = 0; n4 < NC / 4; ++n4)
-            *reinterpret_cast<float4 *>(Gm + tid * NC + 4 * n4) =
-                make_float4(g[4 * n4] + g[NC + 4 * n4], g[4 * n4 + 1] + g[NC + 4 * n4 + 1],
-                            g[4 * n4 + 2] + g[NC + 4 * n4 + 2], g[4 * n4 + 3] + g[NC + 4 * n4 + 3]);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::named_sync(1, kTcThreads);
-      {
-        // parent-path pairs (k_j.k_n, k_j.q_n for j = pj[e]), then the
-        // diagonals k_n.q_n
-        const int npair = off[N];
-        for (int item = tid; item < npair + N; item += kTcThreads) {
-          if (item < npair) {
-            const int n = pn[item];
-            const int j = pj[item];
-            gkk[item] = Gm[j * NC + n];
-            gkq[item] = Gm[j * NC + NMAX + n];
-          } else {
-            const int n = item - npair;
-            kqn[n] = Gm[n * NC + NMAX + n];
-          }
-        }
-      }
-      ptx::named_sync(1, kTcThreads);
-      for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
-        *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
+      wait_on(rec_bar, rec_waits);
     }
 
     // ================= per-tile gates, T and W =================
@@ -663,11 +582,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       bn[nn] = gb;
     }
     ptx::named_sync(1, kTcThreads);
-    const int P = misc[4];
+    const int P = meta[0];
     {
       // one lane per (node n, ancestor-or-self m): column m of T along the
       // stretch m -> n of the parent path (positions 0..L), then W[n][m]
-      const int nl = misc[5];
+      const int nl = meta[1];
       for (int lane_id = tid; lane_id < nl; lane_id += kTcThreads) {
         const int n = ln[lane_id];
         const int L = lane_id - off2[n];
@@ -719,18 +638,19 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (A.status) *A.status = LBX_ETIMEOUT;
       atomicExch(&misc[1], 1);
     }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    {
+      // this thread's 64 columns of the row: hi into A columns hf*32.., lo
+      // into 64 + hf*32..
       uint32_t vh[32], vl[32];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const float4 x4 =
-            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, half * 64 + 4 * q));
+            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, hf * 64 + 4 * q));
         split_bf16x2(x4.x, x4.y, vh[2 * q], vl[2 * q]);
         split_bf16x2(x4.z, x4.w, vh[2 * q + 1], vl[2 * q + 1]);
       }
-      ptx::tmem_st32(tq + Ly::cA1 + half * 32, vh);
-      ptx::tmem_st32(tq + Ly::cA1 + 64 + half * 32, vl);
+      ptx::tmem_st32(tq + Ly::cA1 + hf * 32, vh);
+      ptx::tmem_st32(tq + Ly::cA1 + 64 + hf * 32, vl);
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
@@ -740,19 +660,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     if (lead) {
       // MMA1: [S0 k | S0 q] = S0 [K|Q]^T over K = 128
       ptx::tc_fence_after();
-      mma_kq<NMAX, false>(tmem + Ly::cD1, tmem + Ly::cA1, ptx::smem_u32(B1));
+      mma_kq<NMAX>(tmem + Ly::cD1, tmem + Ly::cA1, ptx::smem_u32(B1));
       ptx::mma_commit(mma_bar);
     }
-    // arrival: this CTA has finished reading the old q/k window of the key
-    // head (its TMA copy completed before S1); the last of the G tiles of
-    // the group writes the new one.  The result is used after the v conv.
-    unsigned int arrived = 0;
-    unsigned int *cnt = A.counters + lb * Hk + kh;
-    if (tid == 32) arrived = atomicAdd(cnt, 1u);
 
-    // ================= v of this row for every node (staged inputs) =================
+    // ================= v of this row for this half's nodes (staged inputs) =================
     wait_on(stg_bar, stg_waits);
-    float vv[NMAX];
+    float vv[NH];
     {
       const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
       const float *cs = reinterpret_cast<const float *>(sg + CS::c);
@@ -762,8 +676,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
         wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
 #pragma unroll
-      for (int n = 0; n < NMAX; ++n) {
-        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * n);
+      for (int i = 0; i < NH; ++i) {
+        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * (n0 + i));
         const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
         float y = 0.f;
 #pragma unroll
@@ -773,74 +687,56 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
           const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
           y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
         }
-        vv[n] = silu_fast(y);
+        vv[i] = silu_fast(y);
       }
       // this row's value channel of the conv window (only this tile reads it)
+      if (hf == 0) {
 #pragma unroll
-      for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
-        if (rr < K - 1) {
-          const int w = crow[rr];
-          const float v = w >= 0 ? bf2f(xs[w * kTcD + r]) : cs[(-1 - w) * kTcD + r];
-          cache_o[(size_t)rr * C + (2 * Hk + h) * kTcD + r] = v;
-        }
+        for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+          if (rr < K - 1) {
+            const int w = crow[rr];
+            const float v = w >= 0 ? bf2f(xs[w * kTcD + r]) : cs[(-1 - w) * kTcD + r];
+            cache_o[(size_t)rr * C + (2 * Hk + h) * kTcD + r] = v;
+          }
+      }
     }
-    if (tid == 32) {
-      const int last = arrived == (unsigned int)(G - 1);
-      if (last) atomicExch(cnt, 0u);
-      misc[2] = last;
-    }
-    ptx::named_sync(1, kTcThreads);  // staging consumed; misc[2] visible
-    if (lead && it + 1 < count) {
-      // next tile's first staging block: its q inputs if it starts a new key
-      // head, else its value-head inputs
-      load_block(t + 1, (t + 1) / G != x.rest ? 0 : 2);
-    }
-    if (misc[2]) {
-      // new q/k window of the key head (this CTA's tile arrived last)
-      const uint16_t *x_lb = A.x + lb * N * C;
-      const float *cache_s = A.conv_cache + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
-      persist_channel_global(kh * kTcD + r, K, C, crow, x_lb, cache_s, cache_o);
-      persist_channel_global((Hk + kh) * kTcD + r, K, C, crow, x_lb, cache_s, cache_o);
-    }
+    ptx::named_sync(1, kTcThreads);  // staging consumed
+    if (lead && it + 1 < count) load_block(t + 1);
 
     // ================= rhs -> tensor memory =================
+    // Accumulator columns are read in aligned blocks of LB covering this
+    // half's nodes; node N0 + i sits at position SH + i of the block.
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
-    float oq[NMAX];
-    {
-      float dv[NC];
+    float oq[NH];
+    auto rhs_half = [&](auto hfc) {
+      constexpr int HF = decltype(hfc)::value;
+      constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
+      constexpr int NL = round_up(SH + NH, LB);
+      float k_hi[NL], k_lo[NL], q_hi[NL], q_lo[NL];
 #pragma unroll
-      for (int c = 0; c < NC / 16; ++c) {
-        float t16[16], u16[16];
-        ptx::tmem_ld16(tq + Ly::cD1 + 16 * c, t16);
-        ptx::tmem_ld16(tq + Ly::cD1 + NC + 16 * c, u16);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) dv[16 * c + e] = t16[e] + u16[e];
+      for (int b = 0; b < NL / LB; ++b) {
+        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + B0 + b * LB, k_hi + b * LB);
+        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + B0 + b * LB, k_lo + b * LB);
+        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NMAX + B0 + b * LB, q_hi + b * LB);
+        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + NMAX + B0 + b * LB, q_lo + b * LB);
       }
+      ptx::tmem_wait_ld();
       // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
-      float rhs[KP];
+      float rhs[NH];
 #pragma unroll
-      for (int n = 0; n < KP; ++n) {
-        if (n < NMAX) {
-          const float ag = an[n] * gam[n];
-          rhs[n] = bn[n] * fmaf(-ag, dv[n], vv[n]);
-          oq[n] = ag * dv[NMAX + n];
-        } else {
-          rhs[n] = 0.f;
-        }
+      for (int i = 0; i < NH; ++i) {
+        const int n = N0 + i;
+        const float ag = an[n] * gam[n];
+        rhs[i] = bn[n] * fmaf(-ag, k_hi[SH + i] + k_lo[SH + i], vv[i]);
+        oq[i] = ag * (q_hi[SH + i] + q_lo[SH + i]);
       }
-      uint32_t rh[KH], rl[KH];
-#pragma unroll
-      for (int e = 0; e < KH; ++e) split_bf16x2(rhs[2 * e], rhs[2 * e + 1], rh[e], rl[e]);
-      if constexpr (KH == 16) {
-        ptx::tmem_st16(tq + Ly::cA2, rh);
-        ptx::tmem_st16(tq + Ly::cA2 + KH, rl);
-      } else {
-        ptx::tmem_st8(tq + Ly::cA2, rh);
-        ptx::tmem_st8(tq + Ly::cA2 + KH, rl);
-      }
-    }
+      store_pairs<NMAX, HF>(tq + Ly::cA2, rhs);
+    };
+    if (hf == 0)
+      rhs_half(std::integral_constant<int, 0>{});
+    else
+      rhs_half(std::integral_constant<int, 1>{});
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S2
@@ -869,34 +765,31 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     // ================= o, path deltas -> tensor memory =================
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
-    {
-      float d2[NC];
+    auto od_half = [&](auto hfc) {
+      constexpr int HF = decltype(hfc)::value;
+      constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
+      constexpr int NL = round_up(SH + NH, LB);
+      float dd[NL], wr[NL];
 #pragma unroll
-      for (int c = 0; c < NC / 16; ++c) {
-        float t16[16];
-        ptx::tmem_ld16(tq + Ly::cD2 + 16 * c, t16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) d2[16 * c + e] = t16[e];
+      for (int b = 0; b < NL / LB; ++b) {
+        ptx::tmem_ld_w<LB>(tq + Ly::cD2 + B0 + b * LB, dd + b * LB);
+        ptx::tmem_ld_w<LB>(tq + Ly::cD2 + NMAX + B0 + b * LB, wr + b * LB);
       }
       ptx::tmem_wait_ld();
       float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
+      float dl[NH];
 #pragma unroll
-      for (int n = 0; n < NMAX; ++n)
-        if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[n] + d2[NMAX + n]);
-      float dl[KP];
-#pragma unroll
-      for (int n = 0; n < KP; ++n) dl[n] = n < NMAX ? cpa[n] * d2[n] : 0.f;
-      uint32_t dh[KH], dlo[KH];
-#pragma unroll
-      for (int e = 0; e < KH; ++e) split_bf16x2(dl[2 * e], dl[2 * e + 1], dh[e], dlo[e]);
-      if constexpr (KH == 16) {
-        ptx::tmem_st16(tq + Ly::cA2, dh);
-        ptx::tmem_st16(tq + Ly::cA2 + KH, dlo);
-      } else {
-        ptx::tmem_st8(tq + Ly::cA2, dh);
-        ptx::tmem_st8(tq + Ly::cA2 + KH, dlo);
+      for (int i = 0; i < NH; ++i) {
+        const int n = N0 + i;
+        if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[i] + wr[SH + i]);
+        dl[i] = cpa[n] * dd[SH + i];
       }
-    }
+      store_pairs<NMAX, HF>(tq + Ly::cA2, dl);
+    };
+    if (hf == 0)
+      od_half(std::integral_constant<int, 0>{});
+    else
+      od_half(std::integral_constant<int, 1>{});
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S3
@@ -922,6 +815,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       }
       ptx::mma_commit(mma_bar);
     }
+    if (lead && it + 1 < count && (t + 1) / G != x.rest) {
+      // the next tile starts a key head: its record replaces this one once
+      // MMA3 (the last reader of the operand) has completed
+      if (ptx::mbar_wait(mma_bar, mma_waits & 1u)) load_rec(t + 1);
+    }
     // gates of the next tile
     if (tid < N && it + 1 < count) {
       const Tile x2 = tile_of(t + 1);
@@ -936,23 +834,16 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       const float gacc = gam[P - 1] * an[P - 1];
       float *srow =
           A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD;
-#pragma unroll 1
-      for (int c64 = 0; c64 < 2; ++c64) {
-        float d[64];
-        {
-          float d0[32], d1[32];
-          ptx::tmem_ld32(tq + Ly::cA1 + 64 * c64, d0);
-          ptx::tmem_ld32(tq + Ly::cA1 + 64 * c64 + 32, d1);
-          ptx::tmem_wait_ld();
+      // this thread's 64 columns, 32 at a time
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            d[e] = d0[e];
-            d[32 + e] = d1[e];
-          }
-        }
+      for (int c = 0; c < 2; ++c) {
+        const int k0 = 64 * hf + 32 * c;
+        float d[32];
+        ptx::tmem_ld32(tq + Ly::cA1 + k0, d);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int k = 64 * c64 + 8 * q;
+        for (int q = 0; q < 4; ++q) {
+          const int k = k0 + 8 * q;
           const float4 a4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k));
           const float4 b4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k + 4));
           stg_v8(srow + k, fmaf(gacc, a4.x, d[8 * q]), fmaf(gacc, a4.y, d[8 * q + 1]),
@@ -965,13 +856,18 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S4
     if (misc[1]) break;
-    if (lead && it + 1 < count) load_state(t + 1);  // the stage has been read
+    if (lead && it + 1 < count) {
+      load_state(t + 1);  // the stage has been read
+      if (tile_of(t + 1).bq != bq) load_tab(t + 1);
+    }
   }
 
   // ---- drain: copies still in flight after an abort ----
   if (lead && misc[1]) {
     if (n_state_loads > 0) (void)ptx::mbar_wait(stage_bar, (uint32_t)((n_state_loads - 1) & 1));
     if (n_stg_loads > 0) (void)ptx::mbar_wait(stg_bar, (uint32_t)((n_stg_loads - 1) & 1));
+    if (n_rec_loads > 0) (void)ptx::mbar_wait(rec_bar, (uint32_t)((n_rec_loads - 1) & 1));
+    if (n_tab_loads > 0) (void)ptx::mbar_wait(tab_bar, (uint32_t)((n_tab_loads - 1) & 1));
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -34,6 +34,17 @@ bool cache_ok(const lbx_cfg *c, const void *p, uintptr_t a) {
   return (c->K == 1 && p == nullptr) || (p != nullptr && aligned(p, a));
 }
 
+// The mode a verify step runs in (LBX_MODE_AUTO resolved).
+int resolve_mode(const lbx_cfg *c) {
+  if (c->mode == LBX_MODE_AUTO) return c->N <= LBX_MAX_TREE_NODES ? LBX_MODE_TREE : LBX_MODE_CHUNKED;
+  return c->mode;
+}
+
+// Whether lbx_verify_step runs the tensor-core step for this configuration.
+bool uses_tc(const lbx_cfg *c) {
+  return resolve_mode(c) == LBX_MODE_TREE && lbx::step_tc_supported(c->d, c->N, 0);
+}
+
 lbx::StepArgs step_args(const lbx_cfg *c) {
   lbx::StepArgs A = {};
   A.L = c->L, A.Bq = c->Bq, A.N = c->N, A.Hk = c->Hk, A.Hv = c->Hv, A.K = c->K;
@@ -44,6 +55,13 @@ lbx::StepArgs step_args(const lbx_cfg *c) {
 }
 
 }  // namespace
+
+namespace lbx {
+size_t counters_bytes(int L, int Bq, int Hk) {
+  const size_t counters = (size_t)L * Bq * Hk * sizeof(unsigned int);
+  return (counters + 255) & ~(size_t)255;
+}
+}  // namespace lbx
 
 extern "C" {
 
@@ -60,8 +78,12 @@ const char *lbx_strerror(int status) {
 
 size_t lbx_workspace_size(const lbx_cfg *cfg) {
   if (check_cfg(cfg) != LBX_OK) return 0;
-  const size_t counters = (size_t)cfg->L * cfg->Bq * cfg->Hk * sizeof(unsigned int);
-  return (counters + 255) & ~(size_t)255;
+  size_t n = lbx::counters_bytes(cfg->L, cfg->Bq, cfg->Hk);
+  if (uses_tc(cfg)) {
+    const size_t tc = lbx::step_tc_workspace_bytes(cfg->L, cfg->Bq, cfg->Hk, cfg->N);
+    n = tc > n ? tc : n;
+  }
+  return n;
 }
 
 int lbx_tree_conv(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_w,
@@ -124,8 +146,7 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
                     cudaStream_t stream) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
-  int mode = cfg->mode;
-  if (mode == LBX_MODE_AUTO) mode = cfg->N <= LBX_MAX_TREE_NODES ? LBX_MODE_TREE : LBX_MODE_CHUNKED;
+  const int mode = resolve_mode(cfg);
   if (mode != LBX_MODE_TREE && mode != LBX_MODE_CHUNKED && mode != LBX_MODE_TREE_CUDA_CORES)
     return LBX_EINVAL;
   if (mode != LBX_MODE_CHUNKED && cfg->N > LBX_MAX_TREE_NODES) return LBX_EINVAL;
@@ -141,8 +162,7 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
   A.parent = parent, A.slot = slot, A.accepted = accepted;
   A.state_in = state, A.state_out = state, A.conv_cache_out = conv_cache;
   A.o = o, A.counters = static_cast<unsigned int *>(workspace), A.status = d_status;
-  if (mode == LBX_MODE_TREE && lbx::step_tc_supported(cfg->d, cfg->N, A.chain))
-    return lbx::launch_step_tc(A, stream);
+  if (uses_tc(cfg)) return lbx::launch_step_tc(A, workspace, workspace_bytes, stream);
   return lbx::launch_step_fused(A, cfg->d, stream);
 }
 

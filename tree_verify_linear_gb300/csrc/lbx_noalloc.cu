@@ -47,7 +47,18 @@ extern "C" int lbx_verify_step_noalloc(const lbx_cfg *cfg, const uint16_t *x,
                                        const int32_t *slot, const int32_t *accepted, float *state,
                                        float *conv_cache, float *o, int32_t *d_status,
                                        cudaStream_t stream) {
-  const size_t need = lbx_workspace_size(cfg);
+  if (cfg == nullptr) return LBX_EINVAL;
+  lbx_cfg c = *cfg;
+  if (lbx_workspace_size(&c) > sizeof(g_noalloc_counters)) {
+    // The tensor-core step keeps per-key-head records in its workspace, far
+    // more than the fixed array holds: run the CUDA-core tree kernel, which
+    // needs only the counters.
+    const int mode = c.mode == LBX_MODE_AUTO
+                         ? (c.N <= LBX_MAX_TREE_NODES ? LBX_MODE_TREE : LBX_MODE_CHUNKED)
+                         : c.mode;
+    if (mode == LBX_MODE_TREE) c.mode = LBX_MODE_TREE_CUDA_CORES;
+  }
+  const size_t need = lbx_workspace_size(&c);
   if (need == 0) return LBX_EINVAL;
   if (need > sizeof(g_noalloc_counters)) return LBX_EINVAL;  // over the fixed capacity
   unsigned int *counters = nullptr;
@@ -56,6 +67,6 @@ extern "C" int lbx_verify_step_noalloc(const lbx_cfg *cfg, const uint16_t *x,
   // The array keeps whatever the previous call left; the counters this call
   // uses must start at zero.
   if (cudaMemsetAsync(counters, 0, need, stream) != cudaSuccess) return LBX_ECUDA;
-  return lbx_verify_step(cfg, x, conv_w, a, b, parent, slot, accepted, state, conv_cache, o,
+  return lbx_verify_step(&c, x, conv_w, a, b, parent, slot, accepted, state, conv_cache, o,
                          counters, need, d_status, stream);
 }

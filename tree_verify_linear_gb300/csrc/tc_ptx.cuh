@@ -147,6 +147,37 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, const uint32_t *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, const uint32_t *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v[0])
+               : "memory");
+}
+// Each lane stores CNT consecutive 32-bit columns, starting OFF columns past
+// an 8-column aligned address, in pieces of 8, 4, 2 or 1 columns that each
+// start at a multiple of their own width.
+template <int OFF, int CNT>
+__device__ __forceinline__ void tmem_st_run(uint32_t taddr, const uint32_t *v) {
+  if constexpr (CNT > 0) {
+    constexpr int P = (CNT >= 8 && OFF % 8 == 0)   ? 8
+                      : (CNT >= 4 && OFF % 4 == 0) ? 4
+                      : (CNT >= 2 && OFF % 2 == 0) ? 2
+                                                   : 1;
+    if constexpr (P == 8) tmem_st8(taddr + OFF, *reinterpret_cast<const uint32_t(*)[8]>(v));
+    if constexpr (P == 4) tmem_st4(taddr + OFF, v);
+    if constexpr (P == 2) tmem_st2(taddr + OFF, v);
+    if constexpr (P == 1) tmem_st1(taddr + OFF, v);
+    tmem_st_run<OFF + P, CNT - P>(taddr, v + P);
+  }
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -164,6 +195,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Each lane loads 8 / 4 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float *v) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Each lane loads W (4, 8, 16 or 32) consecutive 32-bit columns.
+template <int W>
+__device__ __forceinline__ void tmem_ld_w(uint32_t taddr, float *v);
 // Each lane loads 32 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -180,6 +234,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_w<4>(uint32_t taddr, float *v) { tmem_ld4(taddr, v); }
+template <>
+__device__ __forceinline__ void tmem_ld_w<8>(uint32_t taddr, float *v) { tmem_ld8(taddr, v); }
+template <>
+__device__ __forceinline__ void tmem_ld_w<16>(uint32_t taddr, float *v) {
+  tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
+}
+template <>
+__device__ __forceinline__ void tmem_ld_w<32>(uint32_t taddr, float *v) {
+  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(v));
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
