@@ -41,7 +41,7 @@ int launch_step_unfused(const StepArgs &A, int d, cudaStream_t st);
 // head, then the step kernel.  Its workspace holds the prep kernel's tables
 // and records (step_tc_workspace_bytes); no arrival counters.
 bool step_tc_supported(int d, int N, int chain);
-size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int N);
+size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int Hv, int N);
 int launch_step_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Workspace of the CUDA-core fused step: one arrival counter per (layer,

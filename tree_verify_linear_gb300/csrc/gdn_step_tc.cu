@@ -56,7 +56,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *
 
 template <int NMAX>
 int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
-  if (ws == nullptr || ws_bytes < tc_workspace_bytes<NMAX>(A.L, A.Bq, A.Hk)) return LBX_EINVAL;
+  if (ws == nullptr || ws_bytes < tc_workspace_bytes<NMAX>(A.L, A.Bq, A.Hk, A.Hv)) return LBX_EINVAL;
   if (((uintptr_t)ws & 15u) != 0) return LBX_EINVAL;
   if (!have_encode()) return LBX_ECUDA;
   const int nsm = sm_count();
@@ -110,10 +110,10 @@ bool step_tc_supported(int d, int N, int chain) {
   return d == kTcD && !chain && N >= 1 && N <= 24;
 }
 
-size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int N) {
-  if (N <= 8) return tc_workspace_bytes<8>(L, Bq, Hk);
-  if (N <= 16) return tc_workspace_bytes<16>(L, Bq, Hk);
-  if (N <= 24) return tc_workspace_bytes<24>(L, Bq, Hk);
+size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int Hv, int N) {
+  if (N <= 8) return tc_workspace_bytes<8>(L, Bq, Hk, Hv);
+  if (N <= 16) return tc_workspace_bytes<16>(L, Bq, Hk, Hv);
+  if (N <= 24) return tc_workspace_bytes<24>(L, Bq, Hk, Hv);
   return 0;
 }
 

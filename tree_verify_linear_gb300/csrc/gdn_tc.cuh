@@ -75,10 +75,11 @@ struct ConvStage {
 
 // Per-request tree tables in the new labels (built by the prep kernel, one
 // bulk copy into the step kernel): parent-path nodes pj and their node pn per
-// (node, strict ancestor) pair, node ln per (node, ancestor-or-self) lane,
-// parents, depths, pair and lane offsets, conv window sources (input x row
-// >= 0, or cached row -1-w), label maps, new-window sources and
-// {P = accepted-path length, lanes, pairs}.
+// (node, strict ancestor) pair, node ln per (node, ancestor-or-self) lane and
+// the byte offset lofs of the lane's T entry in the [T|W] operand, parents,
+// depths, pair and lane offsets, conv window sources (input x row >= 0, or
+// cached row -1-w), label maps, new-window sources and {P = accepted-path
+// length, lanes, pairs}.
 template <int NMAX>
 struct TabLayout {
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
@@ -86,7 +87,8 @@ struct TabLayout {
   static constexpr int pj = 0;                          // uint8 [kNPair]
   static constexpr int pn = pj + round_up(kNPair, 16);  // uint8 [kNPair]
   static constexpr int ln = pn + round_up(kNPair, 16);  // uint8 [kNLane]
-  static constexpr int par = ln + round_up(kNLane, 16); // int [NMAX]
+  static constexpr int lofs = ln + round_up(kNLane, 16);  // uint16 [kNLane]
+  static constexpr int par = lofs + round_up(2 * kNLane, 16);  // int [NMAX]
   static constexpr int dep = par + 4 * round_up(NMAX, 4);
   static constexpr int off = dep + 4 * round_up(NMAX, 4);      // [NMAX + 4]
   static constexpr int off2 = off + 4 * (NMAX + 4);            // [NMAX + 4]
@@ -99,9 +101,8 @@ struct TabLayout {
   static_assert(win % 16 == 0 && bytes % 16 == 0, "alignment");
 };
 
-// Per-key-head record (built by the prep kernel): the [K|Q] operand image
-// (see TcLayout::b1) followed by the Gram entries k_j.k_n, k_j.q_n of the
-// parent-path pairs and the diagonals k_n.q_n.
+// Gram entries of one key head (prep kernel only): k_j.k_n and k_j.q_n of
+// the parent-path pairs, then the diagonals k_n.q_n.
 template <int NMAX>
 struct GramLayout {
   static constexpr int kNPairP = round_up(NMAX * (NMAX - 1) / 2 + 1, 4);
@@ -109,6 +110,25 @@ struct GramLayout {
   static constexpr int gkq = gkk + 4 * kNPairP;
   static constexpr int kqn = gkq + 4 * kNPairP;
   static constexpr int bytes = kqn + 4 * round_up(NMAX, 4);
+  static_assert(bytes % 16 == 0, "alignment");
+};
+
+// Per-value-head record (built by the prep kernel, bulk-copied per tile):
+// the T and W entries of every (node, ancestor-or-self) lane, and in the new
+// labels the gates a, b, gamma of the parent (product of the ancestors'
+// gates), the accepted-path coefficients g(j->acc), then gamma of the
+// accepted node.
+template <int NMAX>
+struct HeadLayout {
+  static constexpr int kNLaneP = round_up(NMAX * (NMAX + 1) / 2, 4);
+  static constexpr int NP = round_up(NMAX, 4);
+  static constexpr int tw = 0;                 // float [2][kNLaneP]: T, then W
+  static constexpr int an = tw + 8 * kNLaneP;  // float [NP]
+  static constexpr int bn = an + 4 * NP;
+  static constexpr int gam = bn + 4 * NP;
+  static constexpr int cpa = gam + 4 * NP;
+  static constexpr int gacc = cpa + 4 * NP;    // float [4]
+  static constexpr int bytes = gacc + 16;
   static_assert(bytes % 16 == 0, "alignment");
 };
 
@@ -127,56 +147,66 @@ struct TcLayout {
   // columns.
   static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + R1, cD2 = cD1;
   static_assert(cA2 + KP <= kTcTmemCols, "tensor memory");
-  // per-key-head record in the workspace: [K|Q] image, then Gram entries
-  static constexpr int rec_bytes = kB + GramLayout<NMAX>::bytes;
+  // byte distance from a T entry of [T|W] to the W entry of the same lane
+  static constexpr int kWOff = (NMAX / 8) * KP * 16;
+  static_assert(NMAX % 8 == 0, "W rows start at an 8-row group");
   static constexpr int stage = 0;
-  static constexpr int b1 = stage + (int)kStageBytes;  // record: [K|Q] image ...
-  static constexpr int gr = b1 + kB;                   // ... and Gram entries
-  static constexpr int b2hi = gr + GramLayout<NMAX>::bytes;
+  static constexpr int b1 = stage + (int)kStageBytes;  // [K|Q] image of the key head
+  static constexpr int b2hi = b1 + kB;
   static constexpr int b2lo = b2hi + kB2;
-  static constexpr int tf = b2lo + kB2;               // float [NMAX][TP] T scratch
-  static constexpr int stg = round_up(tf + NMAX * TP * 4, 128);  // value-head conv inputs
-  static constexpr int tb = stg + CS::bytes;          // tree tables
-  static constexpr int an = tb + TabLayout<NMAX>::bytes;
-  static constexpr int bn = an + 4 * NMAX;
-  static constexpr int gam = bn + 4 * NMAX;           // gamma of the parent
-  static constexpr int cpa = gam + 4 * NMAX;          // path coefficients g(j->acc)
-  static constexpr int misc = cpa + 4 * NMAX;         // ints, see kernel
-  static constexpr int bars = (misc + 64 + 7) & ~7;   // 5 x uint64
-  static constexpr int total = bars + 5 * 8;
+  static constexpr int stg = round_up(b2lo + kB2, 128);  // value-head conv inputs
+  static constexpr int tb = stg + CS::bytes;           // tree tables
+  static constexpr int hr = tb + TabLayout<NMAX>::bytes;  // value-head record
+  static constexpr int misc = hr + HeadLayout<NMAX>::bytes;  // ints, see kernel
+  static constexpr int bars = (misc + 64 + 7) & ~7;   // 6 x uint64
+  static constexpr int total = bars + 6 * 8;
   static constexpr int smem_bytes = total;
   static_assert(kB % 1024 == 0, "operand [K|Q] must keep 1024-byte alignment");
   static_assert(smem_bytes <= kTcMaxSmem, "two CTAs per SM");
-  static_assert(stg % 128 == 0 && tb % 16 == 0 && b2hi % 16 == 0 && gr % 16 == 0, "alignment");
+  static_assert(stg % 128 == 0 && tb % 16 == 0 && hr % 16 == 0 && b2hi % 16 == 0, "alignment");
 };
 
-// Shared memory of the prep kernel (one CTA per key head).
+// Shared memory of the prep kernel (one CTA per key head).  After the conv
+// the staged inputs are dead and the same bytes hold the per-head T scratch
+// and gate vectors of up to kPrepHeads value heads at a time.
+constexpr int kPrepHeads = 4;
 template <int NMAX>
 struct PrepLayout {
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
-  static constexpr int b1 = 0;                        // [K|Q] image
-  static constexpr int kqf = b1 + Ly::kB;             // fp32 [NC][128]: k rows, then q rows
-  static constexpr int sq = kqf + Ly::NC * kTcD * 4;  // staged q inputs
+  static constexpr int NP = round_up(NMAX, 4);
+  static constexpr int sq = 0;                        // staged q inputs
   static constexpr int sk = sq + CS::bytes;           // staged k inputs
-  static constexpr int gr = sk + CS::bytes;           // Gram entries
+  // reuse of the staging bytes, per head chunk
+  static constexpr int tf = 0;                        // float [kPrepHeads][NMAX][TP]
+  static constexpr int han = tf + kPrepHeads * NMAX * Ly::TP * 4;  // float [kPrepHeads][NP]
+  static constexpr int hbn = han + kPrepHeads * NP * 4;
+  static constexpr int hgam = hbn + kPrepHeads * NP * 4;
+  static_assert(hgam + kPrepHeads * NP * 4 <= 2 * CS::bytes, "head scratch fits the staging");
+  static constexpr int kqf = sk + CS::bytes;          // fp32 [NC][128]: k rows, then q rows
+  static constexpr int gr = kqf + Ly::NC * kTcD * 4;  // Gram entries
   static constexpr int tb = gr + GramLayout<NMAX>::bytes;
   static constexpr int porig = tb + TabLayout<NMAX>::bytes;  // int [NMAX] input parents
-  static constexpr int misc = porig + 4 * round_up(NMAX, 4);
+  static constexpr int misc = porig + 4 * NP;
   static constexpr int bar = (misc + 64 + 7) & ~7;
   static constexpr int total = bar + 8;
   static_assert(sq % 128 == 0 && sk % 128 == 0, "TMA destinations");
 };
 
-// Workspace layout of the tensor-core step: the tree tables of every request,
-// then one record per (layer, request, key head).
+// Workspace layout of the tensor-core step: the tree tables of every
+// request; one [K|Q] image per (layer, request, key head); one value-head
+// record per tile (layer, request, value head), in tile order.
 template <int NMAX>
 __host__ __device__ inline size_t tc_tab_bytes(int Bq) {
   return ((size_t)Bq * TabLayout<NMAX>::bytes + 255) & ~(size_t)255;
 }
 template <int NMAX>
-__host__ __device__ inline size_t tc_workspace_bytes(int L, int Bq, int Hk) {
-  return tc_tab_bytes<NMAX>(Bq) + (size_t)L * Bq * Hk * TcLayout<NMAX>::rec_bytes;
+__host__ __device__ inline size_t tc_head_offset(int L, int Bq, int Hk) {
+  return tc_tab_bytes<NMAX>(Bq) + (size_t)L * Bq * Hk * TcLayout<NMAX>::kB;
+}
+template <int NMAX>
+__host__ __device__ inline size_t tc_workspace_bytes(int L, int Bq, int Hk, int Hv) {
+  return tc_head_offset<NMAX>(L, Bq, Hk) + (size_t)L * Bq * Hv * HeadLayout<NMAX>::bytes;
 }
 
 struct TcArgs {
@@ -253,6 +283,22 @@ __device__ __forceinline__ void conv_weights8(float (&wsl)[8][LBX_MAX_CONV_WIDTH
                                               const unsigned char *cs, int c0) {
   using CS = ConvStage<NMAX>;
   const uint16_t *ws = reinterpret_cast<const uint16_t *>(cs + CS::w);
+  if (K == LBX_MAX_CONV_WIDTH) {
+    // the 8 channels' taps are 64 contiguous bytes: four 16-byte loads
+    // (scalar loads at this lane stride conflict 8-way)
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(ws + c0 * LBX_MAX_CONV_WIDTH);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float t[8];
+      unpack8(w4[q], t);  // channels c0 + 2q, c0 + 2q + 1, taps 0..3 each
+#pragma unroll
+      for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
+        wsl[2 * q][j] = t[LBX_MAX_CONV_WIDTH - 1 - j];
+        wsl[2 * q + 1][j] = t[2 * LBX_MAX_CONV_WIDTH - 1 - j];
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 8; ++e)
 #pragma unroll
@@ -362,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     gdn_step_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
-  constexpr int NC = Ly::NC, R1 = Ly::R1, TP = Ly::TP, KP = Ly::KP, KH = KP / 2;
+  constexpr int NC = Ly::NC, R1 = Ly::R1, KP = Ly::KP, KH = KP / 2;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *st = smem + Ly::stage;
@@ -371,26 +417,19 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   unsigned char *B2hi = smem + Ly::b2hi;
   unsigned char *B2lo = smem + Ly::b2lo;
   using TL = TabLayout<NMAX>;
-  using GL = GramLayout<NMAX>;
-  float *Tf = reinterpret_cast<float *>(smem + Ly::tf);
+  using HL = HeadLayout<NMAX>;
   unsigned char *tb = smem + Ly::tb;
-  const unsigned char *pj = tb + TL::pj;
-  const unsigned char *ln = tb + TL::ln;
-  const int *dep = reinterpret_cast<const int *>(tb + TL::dep);
-  const int *off = reinterpret_cast<const int *>(tb + TL::off);
-  const int *off2 = reinterpret_cast<const int *>(tb + TL::off2);
+  const uint16_t *lofs = reinterpret_cast<const uint16_t *>(tb + TL::lofs);
   const int *win = reinterpret_cast<const int *>(tb + TL::win);
   const int *n2o = reinterpret_cast<const int *>(tb + TL::n2o);
-  const int *o2n = reinterpret_cast<const int *>(tb + TL::o2n);
   const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
   const int *meta = reinterpret_cast<const int *>(tb + TL::meta);  // P, lanes, pairs
-  const float *gkk = reinterpret_cast<const float *>(smem + Ly::gr + GL::gkk);
-  const float *gkq = reinterpret_cast<const float *>(smem + Ly::gr + GL::gkq);
-  const float *kqn = reinterpret_cast<const float *>(smem + Ly::gr + GL::kqn);
-  float *an = reinterpret_cast<float *>(smem + Ly::an);
-  float *bn = reinterpret_cast<float *>(smem + Ly::bn);
-  float *gam = reinterpret_cast<float *>(smem + Ly::gam);
-  float *cpa = reinterpret_cast<float *>(smem + Ly::cpa);
+  unsigned char *hr = smem + Ly::hr;  // value-head record of the current tile
+  const float *tw = reinterpret_cast<const float *>(hr + HL::tw);
+  const float *an = reinterpret_cast<const float *>(hr + HL::an);
+  const float *bn = reinterpret_cast<const float *>(hr + HL::bn);
+  const float *gam = reinterpret_cast<const float *>(hr + HL::gam);
+  const float *cpa = reinterpret_cast<const float *>(hr + HL::cpa);
   int *misc = reinterpret_cast<int *>(smem + Ly::misc);
   // misc[0] error flag, [1] abort, [3] TMEM base
   uint64_t *stage_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);
@@ -398,6 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   uint64_t *mma_bar = stage_bar + 2;
   uint64_t *rec_bar = stage_bar + 3;  // per-key-head record
   uint64_t *tab_bar = stage_bar + 4;  // per-request tables
+  uint64_t *hr_bar = stage_bar + 5;   // per-tile value-head record
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -434,6 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::mbar_init(mma_bar, 1);
     ptx::mbar_init(rec_bar, 1);
     ptx::mbar_init(tab_bar, 1);
+    ptx::mbar_init(hr_bar, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -495,17 +536,21 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
                    (uint32_t)kTcD * K * 2, stg_bar);
     ++n_stg_loads;
   };
-  // the key head's record ([K|Q] image and Gram entries) and the request's
-  // tree tables, from the workspace the prep kernel filled
-  int n_rec_loads = 0, n_tab_loads = 0;
-  const unsigned char *recs = T.ws + tc_tab_bytes<NMAX>(Bq);
+  // the key head's [K|Q] image, the request's tree tables and the tile's
+  // value-head record, from the workspace the prep kernel filled
+  int n_rec_loads = 0, n_tab_loads = 0, n_hr_loads = 0;
+  const unsigned char *imgs = T.ws + tc_tab_bytes<NMAX>(Bq);
+  const unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
   auto load_rec = [&](int t) {
     const Tile x = tile_of(t);
-    const unsigned char *src = recs + (size_t)x.rest * Ly::rec_bytes;
-    ptx::mbar_arrive_expect_tx(rec_bar, (uint32_t)Ly::rec_bytes);
-    ptx::bulk_load(B1, src, (uint32_t)Ly::kB, rec_bar);
-    ptx::bulk_load(smem + Ly::gr, src + Ly::kB, (uint32_t)GL::bytes, rec_bar);
+    ptx::mbar_arrive_expect_tx(rec_bar, (uint32_t)Ly::kB);
+    ptx::bulk_load(B1, imgs + (size_t)x.rest * Ly::kB, (uint32_t)Ly::kB, rec_bar);
     ++n_rec_loads;
+  };
+  auto load_hr = [&](int t) {
+    ptx::mbar_arrive_expect_tx(hr_bar, (uint32_t)HL::bytes);
+    ptx::bulk_load(hr, heads + (size_t)t * HL::bytes, (uint32_t)HL::bytes, hr_bar);
+    ++n_hr_loads;
   };
   auto load_tab = [&](int t) {
     const Tile x = tile_of(t);
@@ -514,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ++n_tab_loads;
   };
   // phases waited for, the same count in every thread
-  uint32_t stg_waits = 0, mma_waits = 0, rec_waits = 0, tab_waits = 0;
+  uint32_t stg_waits = 0, mma_waits = 0, rec_waits = 0, tab_waits = 0, hr_waits = 0;
   auto wait_on = [&](uint64_t *bar, uint32_t &waits) {
     if (!ptx::mbar_wait(bar, waits & 1u)) {
       if (A.status) *A.status = LBX_ETIMEOUT;
@@ -526,6 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   if (lead && count > 0) {
     load_tab(t_begin);
     load_rec(t_begin);
+    load_hr(t_begin);
     load_state(t_begin);
     load_block(t_begin);
   }
@@ -539,14 +585,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   static_assert(NH % 2 == 0, "node halves");
   const int n0 = hf * NH;
   constexpr int LB = NH <= 4 ? 4 : 8;  // accumulator columns per TMEM load
-
-  // gates of the current tile for input node tid (< N), prefetched
-  float ga = 0.f, gb = 0.f;
-  if (tid < N && count > 0) {
-    const Tile x = tile_of(t_begin);
-    ga = bf2f(A.a[((size_t)x.lbi * N + tid) * Hv + x.h]);
-    gb = bf2f(A.b[((size_t)x.lbi * N + tid) * Hv + x.h]);
-  }
 
   int cur_req = -1, cur_group = -1;
   for (int it = 0; it < count; ++it) {
@@ -570,65 +608,21 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       wait_on(rec_bar, rec_waits);
     }
 
-    // ================= per-tile gates, T and W =================
-    if (tid < NMAX && tid >= N) {
-      an[tid] = 0.f;
-      bn[tid] = 0.f;
-      gam[tid] = 0.f;
-    }
-    if (tid < N) {
-      const int nn = o2n[tid];
-      an[nn] = ga;
-      bn[nn] = gb;
-    }
-    ptx::named_sync(1, kTcThreads);
-    const int P = meta[0];
+    // ================= [T | W] of this value head =================
+    wait_on(hr_bar, hr_waits);
+    ptx::named_sync(1, kTcThreads);  // zero-filled [T|W] (new request) before the scatter
+    const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
     {
-      // one lane per (node n, ancestor-or-self m): column m of T along the
-      // stretch m -> n of the parent path (positions 0..L), then W[n][m]
       const int nl = meta[1];
-      for (int lane_id = tid; lane_id < nl; lane_id += kTcThreads) {
-        const int n = ln[lane_id];
-        const int L = lane_id - off2[n];
-        const int e0 = off[n];
-        const int m = L == 0 ? n : pj[e0 + L - 1];
-        Tf[m * TP + m] = 1.f;
-        float xl = 1.f;
-        for (int p = 1; p <= L; ++p) {
-          const int jp = p == L ? n : pj[e0 + (L - p - 1)];
-          const int ep = off[jp];
-          float s = 0.f, g = 1.f;
-          for (int q = p - 1; q >= 0; --q) {
-            const int e = ep + (p - q - 1);
-            const int jq = pj[e];
-            s = fmaf(g * gkk[e], Tf[jq * TP + m], s);
-            g *= an[jq];
-          }
-          xl = -bn[jp] * an[jp] * s;
-          Tf[jp * TP + m] = xl;
-        }
-        float s = 0.f, g = 1.f;
-        for (int q = L - 1; q >= 0; --q) {
-          const int e = e0 + (L - q - 1);
-          const int jq = pj[e];
-          s = fmaf(g * gkq[e], Tf[jq * TP + m], s);
-          g *= an[jq];
-        }
-        const float wv = fmaf(kqn[n], xl, an[n] * s);
-        if (L == dep[n]) gam[n] = g;  // product of the gates of all ancestors
+      for (int lane = tid; lane < nl; lane += kTcThreads) {
+        const uint32_t o = lofs[lane];
         uint16_t th, tl, wh, wl;
-        split_bf16(xl, th, tl);
-        split_bf16(wv, wh, wl);
-        *reinterpret_cast<uint16_t *>(B2hi + plain_bf16(KP, n, m)) = th;
-        *reinterpret_cast<uint16_t *>(B2lo + plain_bf16(KP, n, m)) = tl;
-        *reinterpret_cast<uint16_t *>(B2hi + plain_bf16(KP, NMAX + n, m)) = wh;
-        *reinterpret_cast<uint16_t *>(B2lo + plain_bf16(KP, NMAX + n, m)) = wl;
-      }
-      // accepted-path coefficients g(j->acc) for path nodes j = 0..P-1
-      if (tid < NMAX) {
-        float c = tid < P ? 1.f : 0.f;
-        for (int u = tid + 1; u < P; ++u) c *= an[u];
-        cpa[tid] = c;
+        split_bf16(tw[lane], th, tl);
+        split_bf16(tw[HL::kNLaneP + lane], wh, wl);
+        *reinterpret_cast<uint16_t *>(B2hi + o) = th;
+        *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
+        *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
+        *reinterpret_cast<uint16_t *>(B2lo + o + Ly::kWOff) = wl;
       }
     }
     ptx::fence_proxy_async();
@@ -814,24 +808,20 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         }
       }
       ptx::mma_commit(mma_bar);
+      // every thread has passed its last read of this tile's value-head
+      // record (S3): bring in the next tile's
+      if (it + 1 < count) load_hr(t + 1);
     }
     if (lead && it + 1 < count && (t + 1) / G != x.rest) {
       // the next tile starts a key head: its record replaces this one once
       // MMA3 (the last reader of the operand) has completed
       if (ptx::mbar_wait(mma_bar, mma_waits & 1u)) load_rec(t + 1);
     }
-    // gates of the next tile
-    if (tid < N && it + 1 < count) {
-      const Tile x2 = tile_of(t + 1);
-      ga = bf2f(A.a[((size_t)x2.lbi * N + tid) * Hv + x2.h]);
-      gb = bf2f(A.b[((size_t)x2.lbi * N + tid) * Hv + x2.h]);
-    }
 
     // ================= accepted state row -> global memory =================
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
     {
-      const float gacc = gam[P - 1] * an[P - 1];
       float *srow =
           A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD;
       // this thread's 64 columns, 32 at a time
@@ -868,6 +858,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     if (n_stg_loads > 0) (void)ptx::mbar_wait(stg_bar, (uint32_t)((n_stg_loads - 1) & 1));
     if (n_rec_loads > 0) (void)ptx::mbar_wait(rec_bar, (uint32_t)((n_rec_loads - 1) & 1));
     if (n_tab_loads > 0) (void)ptx::mbar_wait(tab_bar, (uint32_t)((n_tab_loads - 1) & 1));
+    if (n_hr_loads > 0) (void)ptx::mbar_wait(hr_bar, (uint32_t)((n_hr_loads - 1) & 1));
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -1,15 +1,19 @@
 // gdn_tc_prep.cuh -- per-key-head preparation for the tensor-core step.
 //
-// One CTA per (layer l, request b, key head): the q and k conv + SiLU + L2
-// normalisation along each node's ancestor path (q scaled), written as the
-// bf16 hi / lo [K|Q] operand image of the step kernel; the Gram entries
-// k_j.k_n and k_j.q_n of every (node n, strict ancestor j) pair and k_n.q_n
-// (from the same hi + lo values the tensor cores see); the new conv window of
-// the key head's q and k channels, persisted in place (this CTA is the only
-// reader and writer of those channels); and, by the CTAs of layer 0 and key
-// head 0, the request's tree tables.  Everything lands in the caller's
-// workspace and is bulk-copied by the step kernel, so the step kernel's tiles
-// carry no per-key-head prologue and need no arrival counters.
+// One CTA per (layer l, request b, key head) computes what the step kernel's
+// tiles share, so that a tile is only the row work on its state slab:
+//   * the q and k conv + SiLU + L2 normalisation along each node's ancestor
+//     path (q scaled), written to the workspace as the bf16 hi / lo [K|Q]
+//     operand image of the step kernel;
+//   * the Gram entries k_j.k_n, k_j.q_n of every (node n, strict ancestor j)
+//     pair and k_n.q_n, from the same hi + lo values the tensor cores see;
+//   * for each value head of the key head: its gates in the new labels, the
+//     entries of T = (I + diag(b a) M)^-1 and W = Q T on every (node,
+//     ancestor-or-self) lane, gamma of each node's parent, the accepted-path
+//     coefficients and gamma of the accepted node (a value-head record);
+//   * the new conv window of the key head's q and k channels, persisted in
+//     place (this CTA is the only reader and writer of those channels);
+//   * by the CTAs of layer 0 and key head 0, the request's tree tables.
 #pragma once
 
 #include "gdn_tc.cuh"
@@ -20,13 +24,18 @@ constexpr int kPrepThreads = 256;
 
 // Tree tables of one request in the new labels (the accepted path, root
 // first, takes labels 0..P-1; the other nodes follow in input order, so
-// parents still precede children).  All NT threads of the CTA take part;
-// named barrier 1 separates the steps.  porig: int [NMAX] scratch.
-template <int NMAX, int NT>
-__device__ void build_tables(int tid, int N, int K, int acc, const int32_t *par_b,
-                             unsigned char *tb, int *porig) {
+// parents still precede children), built by one warp: lane i holds input
+// node i (N <= NMAX <= 32), ancestor walks are shuffles.  Parent indices
+// that break the tree rules (the step kernel reports such a batch) are
+// clamped so that no index leaves its table.
+template <int NMAX>
+__device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t *par_b,
+                                  unsigned char *tb) {
+  static_assert(NMAX <= 32, "one node per lane");
   using TL = TabLayout<NMAX>;
+  constexpr unsigned FULL = 0xffffffffu;
   unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn, *ln = tb + TL::ln;
+  uint16_t *lofs = reinterpret_cast<uint16_t *>(tb + TL::lofs);
   int *par = reinterpret_cast<int *>(tb + TL::par);
   int *dep = reinterpret_cast<int *>(tb + TL::dep);
   int *off = reinterpret_cast<int *>(tb + TL::off);
@@ -36,127 +45,184 @@ __device__ void build_tables(int tid, int N, int K, int acc, const int32_t *par_
   int *o2n = reinterpret_cast<int *>(tb + TL::o2n);
   int *crow = reinterpret_cast<int *>(tb + TL::crow);
   int *meta = reinterpret_cast<int *>(tb + TL::meta);
-  if (tid < NMAX) {
-    porig[tid] = tid < N ? par_b[tid] : -1;
-    o2n[tid] = -1;
-    n2o[tid] = 0;
-  }
-  ptx::named_sync(1, NT);
-  if (tid == 0) {
-    int P = 0;
-    for (int m = acc; m >= 0; m = porig[m]) ++P;
-    int p = P;
-    for (int m = acc; m >= 0; m = porig[m]) {
-      --p;
-      n2o[p] = m;
-      o2n[m] = p;
-    }
-    int c = P;
-    for (int i = 0; i < N; ++i)
-      if (o2n[i] < 0) {
-        n2o[c] = i;
-        o2n[i] = c;
-        ++c;
+  const bool real = lane < N;
+  int p = real ? par_b[lane] : -1;
+  if (!(p >= 0 && p < lane)) p = -1;
+  if (!(acc >= 0 && acc < N)) acc = 0;
+  // depth: number of strict ancestors
+  int d = 0;
+  {
+    int m = p;
+#pragma unroll 1
+    for (int it = 0; it < NMAX && __any_sync(FULL, m >= 0); ++it) {
+      const int up = __shfl_sync(FULL, p, m >= 0 ? m : 0);
+      if (m >= 0) {
+        ++d;
+        m = up;
       }
-    meta[0] = P;
+    }
   }
-  if (tid == 32) {
-    for (int rr = 0; rr < 4; ++rr) crow[rr] = 0;
-    window_sources(crow, K, acc, porig);
+  // the accepted path (acc and its ancestors): the same walk in every lane
+  bool onp = false;
+  {
+    int c = acc;
+#pragma unroll 1
+    for (int it = 0; it <= NMAX && c >= 0; ++it) {
+      onp |= lane == c;
+      c = __shfl_sync(FULL, p, c);
+    }
   }
-  ptx::named_sync(1, NT);
-  if (tid < NMAX) {
-    // parent, depth and conv window rows in the new labels; taps j >= K
-    // and padding nodes point at input row 0
-    const int o = tid < N ? n2o[tid] : 0;
-    par[tid] = tid < N && porig[o] >= 0 ? o2n[porig[o]] : -1;
-    int d = 0;
-    if (tid < N)
-      for (int m = porig[o]; m >= 0; m = porig[m]) ++d;
-    dep[tid] = d;
-    int m = tid < N ? o : -2, past = 0;
+  const unsigned pathm = __ballot_sync(FULL, onp && real);
+  const unsigned restm = __ballot_sync(FULL, !onp && real);
+  const int P = __popc(pathm);
+  // new label: depth on the path, else after the path in input order
+  const int nlab = onp ? d : P + __popc(restm & ((1u << lane) - 1u));
+  const int newp_src = __shfl_sync(FULL, nlab, p >= 0 ? p : 0);
+  // conv window rows (input labels) of each node: itself, then ancestors,
+  // then cached rows (-1 - row); taps j >= K and padding nodes read row 0
+  int wj[4];
+  {
+    int m = real ? lane : -2, past = 0;
+#pragma unroll
     for (int j = 0; j < 4; ++j) {
       int w = 0;
-      if (tid < N && j < K) {
+      if (real && j < K) {
         if (m >= 0) {
           w = m;
-          m = porig[m];
         } else {
           ++past;
           w = -1 - (K - 1 - past);
         }
       }
-      win[tid * 4 + j] = w;
+      wj[j] = w;
+      const int up = __shfl_sync(FULL, p, m >= 0 ? m : 0);
+      if (real && j < K && m >= 0) m = up;
     }
   }
-  ptx::named_sync(1, NT);
-  if (tid <= NMAX) {
-    int o1 = 0, o2 = 0;
-    for (int i = 0; i < N && i < tid; ++i) {
-      o1 += dep[i];
-      o2 += dep[i] + 1;
-    }
-    off[tid] = o1;
-    off2[tid] = o2;
+  if (real) {
+    n2o[nlab] = lane;
+    o2n[lane] = nlab;
+    par[nlab] = p >= 0 ? newp_src : -1;
+    dep[nlab] = d;
+    *reinterpret_cast<int4 *>(win + 4 * nlab) = make_int4(wj[0], wj[1], wj[2], wj[3]);
+  } else if (lane < NMAX) {
+    n2o[lane] = 0;
+    o2n[lane] = -1;
+    par[lane] = -1;
+    dep[lane] = 0;
+    *reinterpret_cast<int4 *>(win + 4 * lane) = make_int4(0, 0, 0, 0);
   }
-  ptx::named_sync(1, NT);
-  for (int i = tid; i < N; i += NT) {
-    int j = par[i];
-    for (int e = off[i]; e < off[i + 1]; ++e) {
-      pj[e] = (unsigned char)j;
-      pn[e] = (unsigned char)i;
-      j = par[j];
+  // new-window sources of the persist: row rr takes the (K-2-rr)-th
+  // ancestor of acc, or old cache row depth(acc)+1+rr where the path is short
+  {
+    const int da = __shfl_sync(FULL, d, acc);
+    int src[3] = {0, 0, 0};
+    int m = acc;
+#pragma unroll
+    for (int step = 0; step < 3; ++step) {  // m = step-th ancestor of acc
+#pragma unroll
+      for (int rr = 0; rr < 3; ++rr)
+        if (rr < K - 1 && K - 2 - rr == step && step <= da) src[rr] = m;
+      m = __shfl_sync(FULL, p, m >= 0 ? m : 0);
     }
-    for (int q = off2[i]; q < off2[i + 1]; ++q) ln[q] = (unsigned char)i;
+#pragma unroll
+    for (int rr = 0; rr < 3; ++rr)
+      if (rr < K - 1 && K - 2 - rr > da) src[rr] = -1 - (da + 1 + rr);
+    if (lane == 0) {
+      for (int rr = 0; rr < 4; ++rr) crow[rr] = rr < 3 && rr < K - 1 ? src[rr] : 0;
+    }
   }
-  if (tid == 0) {
-    meta[1] = off2[N];
-    meta[2] = off[N];
+  __syncwarp();
+  // parent-path and lane offsets in the new labels (lane = new label)
+  const int dl = lane < N ? dep[lane] : 0;
+  const int pl = lane < N ? par[lane] : -1;
+  int s1 = dl, s2 = lane < N ? dl + 1 : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t1 = __shfl_up_sync(FULL, s1, o), t2 = __shfl_up_sync(FULL, s2, o);
+    if (lane >= o) {
+      s1 += t1;
+      s2 += t2;
+    }
+  }
+  const int e1 = s1 - dl, e2 = s2 - (lane < N ? dl + 1 : 0);  // exclusive prefix
+  if (lane <= NMAX) {
+    off[lane] = e1;
+    off2[lane] = e2;
+  }
+  if (lane == N) {
+    meta[0] = P;
+    meta[1] = e2;
+    meta[2] = e1;
     meta[3] = 0;
   }
-  ptx::named_sync(1, NT);
+  // pairs (node, strict ancestor) and lanes (node, ancestor-or-self)
+  {
+    int j = pl, t = 0;
+    if (lane < N) {
+      ln[e2] = (unsigned char)lane;
+      lofs[e2] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, lane, lane);
+    }
+#pragma unroll 1
+    for (int it = 0; it < NMAX && __any_sync(FULL, j >= 0); ++it) {
+      if (lane < N && j >= 0) {
+        pj[e1 + t] = (unsigned char)j;
+        pn[e1 + t] = (unsigned char)lane;
+        ln[e2 + t + 1] = (unsigned char)lane;
+        lofs[e2 + t + 1] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, lane, j);
+        ++t;
+      }
+      const int up = __shfl_sync(FULL, pl, j >= 0 ? j : 0);
+      if (j >= 0) j = up;
+    }
+  }
+  __syncwarp();
 }
 
 template <int NMAX>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 4)
     gdn_qk_prep_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using PL = PrepLayout<NMAX>;
   using CS = ConvStage<NMAX>;
   using TL = TabLayout<NMAX>;
   using GL = GramLayout<NMAX>;
-  constexpr int NT = kPrepThreads, NC = Ly::NC, R1 = Ly::R1;
+  using HL = HeadLayout<NMAX>;
+  constexpr int NT = kPrepThreads, NC = Ly::NC, R1 = Ly::R1, TP = Ly::TP, NP = PL::NP;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *B1 = smem + PL::b1;
-  float *kqf = reinterpret_cast<float *>(smem + PL::kqf);
   unsigned char *sq = smem + PL::sq, *sk = smem + PL::sk;
+  float *kqf = reinterpret_cast<float *>(smem + PL::kqf);
   float *gkk = reinterpret_cast<float *>(smem + PL::gr + GL::gkk);
   float *gkq = reinterpret_cast<float *>(smem + PL::gr + GL::gkq);
   float *kqn = reinterpret_cast<float *>(smem + PL::gr + GL::kqn);
   unsigned char *tb = smem + PL::tb;
-  int *porig = reinterpret_cast<int *>(smem + PL::porig);
   int *misc = reinterpret_cast<int *>(smem + PL::misc);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + PL::bar);
+  // per-head scratch, in the staging bytes once the conv is done
+  float *Tf = reinterpret_cast<float *>(smem + PL::tf);
+  float *han = reinterpret_cast<float *>(smem + PL::han);
+  float *hbn = reinterpret_cast<float *>(smem + PL::hbn);
+  float *hgam = reinterpret_cast<float *>(smem + PL::hgam);
   const int tid = threadIdx.x;
   const int N = A.N, K = A.K, Hk = A.Hk, Hv = A.Hv, Bq = A.Bq;
+  const int G = Hv / Hk;
   const int C = (2 * Hk + Hv) * kTcD;
   const uint32_t stg_bytes =
       (uint32_t)N * kTcD * 2 + (uint32_t)(K - 1) * kTcD * 4 + (uint32_t)kTcD * K * 2;
 
-  // an invalid batch is reported by the step kernel; nothing is done here
-  {
-    const int code =
-        validate_batch(A.parent, A.slot, A.accepted, Bq, N, A.n_slots, false, true, true);
-    if (block_any_error(code, misc)) return;
-  }
   const int g = blockIdx.x;
   const int kh = g % Hk, lbi = g / Hk;
   const int bq = lbi % Bq, l = lbi / Bq;
-  const int slot_b = A.slot[bq];
-  const int crow0 = (l * A.n_slots + slot_b) * (K - 1);
+  unsigned char *img = T.ws + tc_tab_bytes<NMAX>(Bq) + (size_t)g * Ly::kB;
+  unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
 
+  // The copies only read, so they start before the batch is validated (an
+  // out-of-range slot is clamped here; such a batch is rejected below).
+  int slot_b = A.slot[bq];
+  slot_b = slot_b < 0 ? 0 : (slot_b >= A.n_slots ? A.n_slots - 1 : slot_b);
   if (tid == 0) {
+    const int crow0 = (l * A.n_slots + slot_b) * (K - 1);
     ptx::mbar_init(bar, 1);
     ptx::fence_mbar_init();
     ptx::mbar_arrive_expect_tx(bar, 2 * stg_bytes);
@@ -169,19 +235,34 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                      (uint32_t)kTcD * K * 2, bar);
     }
   }
-  __syncthreads();
-  build_tables<NMAX, NT>(tid, N, K, A.accepted[bq], A.parent + (size_t)bq * N, tb, porig);
+  // tables (warp 0) while the copies fly; an invalid batch is reported by
+  // the step kernel, and nothing is written here
+  if (tid < 32) build_tables_warp<NMAX>(tid, N, K, A.accepted[bq], A.parent + (size_t)bq * N, tb);
+  {
+    const int code =
+        validate_batch(A.parent, A.slot, A.accepted, Bq, N, A.n_slots, false, true, true);
+    if (block_any_error(code, misc)) {
+      if (tid == 0) (void)ptx::mbar_wait(bar, 0);  // the copies land before the CTA exits
+      return;
+    }
+  }
   const int *win = reinterpret_cast<const int *>(tb + TL::win);
   const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
-  const unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn;
-  const int npair = reinterpret_cast<const int *>(tb + TL::meta)[2];
+  const int *dep = reinterpret_cast<const int *>(tb + TL::dep);
+  const int *off = reinterpret_cast<const int *>(tb + TL::off);
+  const int *off2 = reinterpret_cast<const int *>(tb + TL::off2);
+  const int *n2o = reinterpret_cast<const int *>(tb + TL::n2o);
+  const unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn, *ln = tb + TL::ln;
+  const int *meta = reinterpret_cast<const int *>(tb + TL::meta);
+  const int P = meta[0], nl = meta[1], npair = meta[2];
   if (!ptx::mbar_wait(bar, 0)) {
     if (A.status) *A.status = LBX_ETIMEOUT;
     (void)ptx::mbar_wait(bar, 0);  // the copies must land before the CTA exits
     return;
   }
 
-  // q, then k: conv + SiLU + L2 norm -> operand rows (hi, lo) and fp32 hi + lo
+  // q, then k: conv + SiLU + L2 norm -> operand rows (hi, lo) of the image in
+  // the workspace, and their fp32 values hi + lo for the Gram entries
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
     const unsigned char *cs = which == 0 ? sq : sk;
@@ -215,9 +296,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           kv[2 * e + 1] =
               __uint_as_float(wh[e] & 0xffff0000u) + __uint_as_float(wl[e] & 0xffff0000u);
         }
-        *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, li * 8)) =
+        *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, brow, li * 8)) =
             make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, li * 8)) =
+        *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, li * 8)) =
             make_uint4(wl[0], wl[1], wl[2], wl[3]);
         float4 *kd = reinterpret_cast<float4 *>(kqf + brow * kTcD + li * 8);
         kd[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
@@ -227,9 +308,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     // padding rows of this half of the operand are zero
     for (int idx = tid; idx < (NMAX - N) * 16; idx += NT) {
       const int brow = (which == 0 ? NMAX : 0) + N + idx / 16;
-      *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, brow, 8 * (idx % 16))) =
+      *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, brow, 8 * (idx % 16))) =
           make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(B1 + sw128_bf16(R1, NC + brow, 8 * (idx % 16))) =
+      *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, 8 * (idx % 16))) =
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
@@ -247,7 +328,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       cache_o[(size_t)rr * C + gc] = w >= 0 ? bf2f(xs[w * kTcD + c]) : cc[(-1 - w) * kTcD + c];
     }
   }
-  __syncthreads();
+  __syncthreads();  // the staged inputs are dead from here on
   {
     // Gram entries, 8 threads per item: the parent-path pairs, then the
     // diagonals
@@ -291,17 +372,88 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
   }
   __syncthreads();
-  {
-    // record -> workspace (and the request's tables, once per request)
-    uint4 *rec = reinterpret_cast<uint4 *>(T.ws + tc_tab_bytes<NMAX>(Bq) +
-                                           (size_t)g * Ly::rec_bytes);
-    for (int i = tid; i < Ly::kB / 16; i += NT) rec[i] = reinterpret_cast<const uint4 *>(B1)[i];
-    for (int i = tid; i < GL::bytes / 16; i += NT)
-      rec[Ly::kB / 16 + i] = reinterpret_cast<const uint4 *>(smem + PL::gr)[i];
-    if (l == 0 && kh == 0) {
-      uint4 *tab = reinterpret_cast<uint4 *>(T.ws + (size_t)bq * TL::bytes);
-      for (int i = tid; i < TL::bytes / 16; i += NT) tab[i] = reinterpret_cast<const uint4 *>(tb)[i];
+
+  // ---- the G value heads of this key head, kPrepHeads at a time ----
+#pragma unroll 1
+  for (int hc = 0; hc < G; hc += kPrepHeads) {
+    const int nh = G - hc < kPrepHeads ? G - hc : kPrepHeads;
+    // gates of head hc + hh in the new labels (0 for padding nodes)
+    for (int idx = tid; idx < kPrepHeads * NP; idx += NT) {
+      const int hh = idx / NP, n = idx % NP;
+      float av = 0.f, bv = 0.f;
+      if (hh < nh && n < N) {
+        const size_t gi = ((size_t)lbi * N + n2o[n]) * Hv + kh * G + hc + hh;
+        av = bf2f(A.a[gi]);
+        bv = bf2f(A.b[gi]);
+      }
+      han[idx] = av;
+      hbn[idx] = bv;
+      hgam[idx] = 0.f;
     }
+    __syncthreads();
+    // one task per (head, node n, ancestor-or-self m): column m of T along
+    // the stretch m -> n of the parent path (positions 0..L), then W[n][m]
+    for (int task = tid; task < nh * nl; task += NT) {
+      const int hh = task / nl, lane = task - hh * nl;
+      const float *an = han + hh * NP, *bn = hbn + hh * NP;
+      float *tf = Tf + hh * NMAX * TP;
+      const int n = ln[lane];
+      const int L = lane - off2[n];
+      const int e0 = off[n];
+      const int m = L == 0 ? n : pj[e0 + L - 1];
+      tf[m * TP + m] = 1.f;
+      float xl = 1.f;
+      for (int p = 1; p <= L; ++p) {
+        const int jp = p == L ? n : pj[e0 + (L - p - 1)];
+        const int ep = off[jp];
+        float s = 0.f, gp = 1.f;
+        for (int q = p - 1; q >= 0; --q) {
+          const int e = ep + (p - q - 1);
+          const int jq = pj[e];
+          s = fmaf(gp * gkk[e], tf[jq * TP + m], s);
+          gp *= an[jq];
+        }
+        xl = -bn[jp] * an[jp] * s;
+        tf[jp * TP + m] = xl;
+      }
+      float s = 0.f, gp = 1.f;
+      for (int q = L - 1; q >= 0; --q) {
+        const int e = e0 + (L - q - 1);
+        const int jq = pj[e];
+        s = fmaf(gp * gkq[e], tf[jq * TP + m], s);
+        gp *= an[jq];
+      }
+      float *hrec = reinterpret_cast<float *>(
+          heads + ((size_t)lbi * Hv + kh * G + hc + hh) * HL::bytes + HL::tw);
+      hrec[lane] = xl;
+      hrec[HL::kNLaneP + lane] = fmaf(kqn[n], xl, an[n] * s);
+      if (L == dep[n]) hgam[hh * NP + n] = gp;  // product of the gates of all ancestors
+    }
+    __syncthreads();
+    // gates, gamma, accepted-path coefficients g(j->acc) (path = labels
+    // 0..P-1) and gamma of the accepted node
+    for (int idx = tid; idx < nh * NP; idx += NT) {
+      const int hh = idx / NP, n = idx % NP;
+      const float *an = han + hh * NP;
+      unsigned char *hb = heads + ((size_t)lbi * Hv + kh * G + hc + hh) * HL::bytes;
+      float c = n < P ? 1.f : 0.f;
+      for (int u = n + 1; u < P; ++u) c *= an[u];
+      reinterpret_cast<float *>(hb + HL::an)[n] = an[n];
+      reinterpret_cast<float *>(hb + HL::bn)[n] = hbn[idx];
+      reinterpret_cast<float *>(hb + HL::gam)[n] = hgam[idx];
+      reinterpret_cast<float *>(hb + HL::cpa)[n] = c;
+      if (n == 0) {
+        float4 *ga = reinterpret_cast<float4 *>(hb + HL::gacc);
+        *ga = make_float4(hgam[hh * NP + P - 1] * an[P - 1], 0.f, 0.f, 0.f);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (l == 0 && kh == 0) {
+    // the request's tree tables, once per request
+    uint4 *tab = reinterpret_cast<uint4 *>(T.ws + (size_t)bq * TL::bytes);
+    for (int i = tid; i < TL::bytes / 16; i += NT) tab[i] = reinterpret_cast<const uint4 *>(tb)[i];
   }
 }
 

@@ -80,7 +80,7 @@ size_t lbx_workspace_size(const lbx_cfg *cfg) {
   if (check_cfg(cfg) != LBX_OK) return 0;
   size_t n = lbx::counters_bytes(cfg->L, cfg->Bq, cfg->Hk);
   if (uses_tc(cfg)) {
-    const size_t tc = lbx::step_tc_workspace_bytes(cfg->L, cfg->Bq, cfg->Hk, cfg->N);
+    const size_t tc = lbx::step_tc_workspace_bytes(cfg->L, cfg->Bq, cfg->Hk, cfg->Hv, cfg->N);
     n = tc > n ? tc : n;
   }
   return n;
