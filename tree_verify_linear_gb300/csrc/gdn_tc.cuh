@@ -502,6 +502,23 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     x.h = x.kh * G + x.hg;
     return x;
   };
+  // the tile after x (tiles are visited in order)
+  auto next_tile = [&](Tile x) {
+    if (++x.hg == G) {
+      x.hg = 0;
+      ++x.rest;
+      if (++x.kh == Hk) {
+        x.kh = 0;
+        ++x.lbi;
+        if (++x.bq == Bq) {
+          x.bq = 0;
+          ++x.l;
+        }
+      }
+    }
+    x.h = x.kh * G + x.hg;
+    return x;
+  };
   // cache slot of a request, read from global memory once per request
   struct SlotCache {
     int bq = -1, slot = 0;
@@ -516,8 +533,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   SlotCache lead_slots, tile_slots;
   // lead thread: copies into the stage and the staging buffer
   int n_state_loads = 0, n_stg_loads = 0;
-  auto load_state = [&](int t) {
-    const Tile x = tile_of(t);
+  auto load_state = [&](const Tile &x) {
     const int srow = ((x.l * A.n_slots + slot_of(lead_slots, x.bq)) * Hv + x.h) * kTcD;
     ptx::mbar_arrive_expect_tx(stage_bar, kStageBytes);
     for (int a = 0; a < 4; ++a)
@@ -525,8 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ++n_state_loads;
   };
   // conv inputs of the value head's channels
-  auto load_block = [&](int t) {
-    const Tile x = tile_of(t);
+  auto load_block = [&](const Tile &x) {
     const int ch0 = (2 * Hk + x.h) * kTcD;
     const int crow0 = (x.l * A.n_slots + slot_of(lead_slots, x.bq)) * (K - 1);
     ptx::mbar_arrive_expect_tx(stg_bar, stg_bytes);
@@ -541,8 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   int n_rec_loads = 0, n_tab_loads = 0, n_hr_loads = 0;
   const unsigned char *imgs = T.ws + tc_tab_bytes<NMAX>(Bq);
   const unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
-  auto load_rec = [&](int t) {
-    const Tile x = tile_of(t);
+  auto load_rec = [&](const Tile &x) {
     ptx::mbar_arrive_expect_tx(rec_bar, (uint32_t)Ly::kB);
     ptx::bulk_load(B1, imgs + (size_t)x.rest * Ly::kB, (uint32_t)Ly::kB, rec_bar);
     ++n_rec_loads;
@@ -552,8 +566,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::bulk_load(hr, heads + (size_t)t * HL::bytes, (uint32_t)HL::bytes, hr_bar);
     ++n_hr_loads;
   };
-  auto load_tab = [&](int t) {
-    const Tile x = tile_of(t);
+  auto load_tab = [&](const Tile &x) {
     ptx::mbar_arrive_expect_tx(tab_bar, (uint32_t)TL::bytes);
     ptx::bulk_load(tb, T.ws + (size_t)x.bq * TL::bytes, (uint32_t)TL::bytes, tab_bar);
     ++n_tab_loads;
@@ -568,12 +581,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ++waits;
   };
 
+  Tile cur = tile_of(t_begin);
   if (lead && count > 0) {
-    load_tab(t_begin);
-    load_rec(t_begin);
+    load_tab(cur);
+    load_rec(cur);
     load_hr(t_begin);
-    load_state(t_begin);
-    load_block(t_begin);
+    load_state(cur);
+    load_block(cur);
   }
 
   // state row r (= TMEM lane) and half hf of this thread; the row work of
@@ -589,7 +603,9 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   int cur_req = -1, cur_group = -1;
   for (int it = 0; it < count; ++it) {
     const int t = t_begin + it;
-    const Tile x = tile_of(t);
+    const Tile x = cur;
+    const Tile nx = next_tile(x);
+    cur = nx;
     const int bq = x.bq, l = x.l, h = x.h;
     const size_t lb = (size_t)x.lbi;
     const int slot_b = slot_of(tile_slots, bq);
@@ -695,7 +711,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       }
     }
     ptx::named_sync(1, kTcThreads);  // staging consumed
-    if (lead && it + 1 < count) load_block(t + 1);
+    if (lead && it + 1 < count) load_block(nx);
 
     // ================= rhs -> tensor memory =================
     // Accumulator columns are read in aligned blocks of LB covering this
@@ -731,10 +747,27 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       rhs_half(std::integral_constant<int, 0>{});
     else
       rhs_half(std::integral_constant<int, 1>{});
+    // gamma_acc S0 into the MMA3 accumulator (the S0 columns, free since
+    // MMA1 completed), this thread's 64 columns; the stage is not read again
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int k0 = 64 * hf + 32 * c;
+      uint32_t gs[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k0 + 4 * q));
+        gs[4 * q] = __float_as_uint(gacc * s4.x);
+        gs[4 * q + 1] = __float_as_uint(gacc * s4.y);
+        gs[4 * q + 2] = __float_as_uint(gacc * s4.z);
+        gs[4 * q + 3] = __float_as_uint(gacc * s4.w);
+      }
+      ptx::tmem_st32(tq + Ly::cA1 + k0, gs);
+    }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S2
     if (misc[1]) break;
+    if (lead && it + 1 < count) load_state(nx);  // the stage has been read
     if (lead) {
       // MMA2: [delta | W rhs] = rhs [T|W]^T, three passes over K = KP
       ptx::tc_fence_after();
@@ -794,7 +827,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kTcD);
       const uint32_t b1_a = ptx::smem_u32(B1);
-      uint32_t accum = 0;
+      uint32_t accum = 1;  // onto gamma_acc S0
 #pragma unroll 1
       for (int pass = 0; pass < 3; ++pass) {
         const uint32_t a_col = Ly::cA2 + (pass == 2 ? KH : 0);
@@ -812,13 +845,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       // record (S3): bring in the next tile's
       if (it + 1 < count) load_hr(t + 1);
     }
-    if (lead && it + 1 < count && (t + 1) / G != x.rest) {
+    if (lead && it + 1 < count && nx.rest != x.rest) {
       // the next tile starts a key head: its record replaces this one once
       // MMA3 (the last reader of the operand) has completed
-      if (ptx::mbar_wait(mma_bar, mma_waits & 1u)) load_rec(t + 1);
+      if (ptx::mbar_wait(mma_bar, mma_waits & 1u)) load_rec(nx);
     }
 
-    // ================= accepted state row -> global memory =================
+    // ================= accepted state row (gamma_acc S0 + MMA3) -> global memory =================
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
     {
@@ -832,24 +865,15 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         ptx::tmem_ld32(tq + Ly::cA1 + k0, d);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int k = k0 + 8 * q;
-          const float4 a4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k));
-          const float4 b4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k + 4));
-          stg_v8(srow + k, fmaf(gacc, a4.x, d[8 * q]), fmaf(gacc, a4.y, d[8 * q + 1]),
-                 fmaf(gacc, a4.z, d[8 * q + 2]), fmaf(gacc, a4.w, d[8 * q + 3]),
-                 fmaf(gacc, b4.x, d[8 * q + 4]), fmaf(gacc, b4.y, d[8 * q + 5]),
-                 fmaf(gacc, b4.z, d[8 * q + 6]), fmaf(gacc, b4.w, d[8 * q + 7]));
-        }
+        for (int q = 0; q < 4; ++q)
+          stg_v8(srow + k0 + 8 * q, d[8 * q], d[8 * q + 1], d[8 * q + 2], d[8 * q + 3],
+                 d[8 * q + 4], d[8 * q + 5], d[8 * q + 6], d[8 * q + 7]);
       }
     }
     ptx::tc_fence_before();
     __syncthreads();  // ---------------------------------------------- S4
     if (misc[1]) break;
-    if (lead && it + 1 < count) {
-      load_state(t + 1);  // the stage has been read
-      if (tile_of(t + 1).bq != bq) load_tab(t + 1);
-    }
+    if (lead && it + 1 < count && nx.bq != bq) load_tab(nx);
   }
 
   // ---- drain: copies still in flight after an abort ----
