@@ -100,7 +100,19 @@ int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
     return LBX_ECUDA;
   const int slots = kTcCtasPerSm * nsm;
   const int grid = T.n_tiles < slots ? T.n_tiles : slots;
-  kern<<<grid, kTcThreads, smem, st>>>(maps, T);
+  // programmatic stream serialization: the step kernel may start while the
+  // prep kernel's last CTAs run, and waits for it before reading the workspace
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(kTcThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, kern, maps, T) != cudaSuccess) return LBX_ECUDA;
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
 

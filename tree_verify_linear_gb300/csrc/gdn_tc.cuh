@@ -78,8 +78,9 @@ struct ConvStage {
 // (node, strict ancestor) pair, node ln per (node, ancestor-or-self) lane and
 // the byte offset lofs of the lane's T entry in the [T|W] operand, parents,
 // depths, pair and lane offsets, conv window sources (input x row >= 0, or
-// cached row -1-w), label maps, new-window sources and {P = accepted-path
-// length, lanes, pairs}.
+// cached row -1-w), label maps, the nodes in conv order (those whose window
+// lies inside the tree first), new-window sources and {P = accepted-path
+// length, lanes, pairs, nodes whose window lies inside the tree}.
 template <int NMAX>
 struct TabLayout {
   static constexpr int kNPair = NMAX * (NMAX - 1) / 2 + 1;
@@ -95,7 +96,8 @@ struct TabLayout {
   static constexpr int win = off2 + 4 * (NMAX + 4);            // [NMAX][4]
   static constexpr int n2o = win + 16 * NMAX;
   static constexpr int o2n = n2o + 4 * round_up(NMAX, 4);
-  static constexpr int crow = o2n + 4 * round_up(NMAX, 4);     // [4]
+  static constexpr int corder = o2n + 4 * round_up(NMAX, 4);  // [NMAX] conv order
+  static constexpr int crow = corder + 4 * round_up(NMAX, 4);  // [4]
   static constexpr int meta = crow + 16;                       // [4] P, lanes, pairs
   static constexpr int bytes = meta + 16;
   static_assert(win % 16 == 0 && bytes % 16 == 0, "alignment");
@@ -183,8 +185,9 @@ struct PrepLayout {
   static constexpr int hbn = han + kPrepHeads * NP * 4;
   static constexpr int hgam = hbn + kPrepHeads * NP * 4;
   static_assert(hgam + kPrepHeads * NP * 4 <= 2 * CS::bytes, "head scratch fits the staging");
-  static constexpr int kqf = sk + CS::bytes;          // fp32 [NC][128]: k rows, then q rows
-  static constexpr int gr = kqf + Ly::NC * kTcD * 4;  // Gram entries
+  static constexpr int KQP = kTcD + 4;               // padded row pitch (bank spread)
+  static constexpr int kqf = sk + CS::bytes;          // fp32 [NC][KQP]: k rows, then q rows
+  static constexpr int gr = kqf + Ly::NC * KQP * 4;   // Gram entries
   static constexpr int tb = gr + GramLayout<NMAX>::bytes;
   static constexpr int porig = tb + TabLayout<NMAX>::bytes;  // int [NMAX] input parents
   static constexpr int misc = porig + 4 * NP;
@@ -333,6 +336,29 @@ __device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win,
     const float xc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = fmaf(wsl[e][j], row >= 0 ? xn[e] : xc[e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) out[e] = silu_fast(acc[e]);
+}
+
+// conv8_staged for a node whose window lies inside the tree (every row
+// >= 0): no cached-row loads, no selects.
+template <int NMAX>
+__device__ __forceinline__ void conv8_staged_tree(float (&out)[8], const int *win,
+                                                  const float (&wsl)[8][LBX_MAX_CONV_WIDTH],
+                                                  const unsigned char *cs, int c0) {
+  using CS = ConvStage<NMAX>;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const int4 w4 = *reinterpret_cast<const int4 *>(win);
+  const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+  for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
+    float xn[8];
+    unpack8(*reinterpret_cast<const uint4 *>(cs + CS::x + wj[j] * kTcD * 2 + c0 * 2), xn);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wsl[e][j], xn[e], acc[e]);
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) out[e] = silu_fast(acc[e]);
@@ -583,11 +609,14 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 
   Tile cur = tile_of(t_begin);
   if (lead && count > 0) {
+    // the state and the value-head inputs are not written by the prep
+    // kernel: they load while it finishes; the workspace only after it
+    load_state(cur);
+    load_block(cur);
+    ptx::wait_prerequisite_grid();
     load_tab(cur);
     load_rec(cur);
     load_hr(t_begin);
-    load_state(cur);
-    load_block(cur);
   }
 
   // state row r (= TMEM lane) and half hf of this thread; the row work of

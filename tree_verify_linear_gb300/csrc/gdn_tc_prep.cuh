@@ -43,6 +43,7 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
   int *win = reinterpret_cast<int *>(tb + TL::win);
   int *n2o = reinterpret_cast<int *>(tb + TL::n2o);
   int *o2n = reinterpret_cast<int *>(tb + TL::o2n);
+  int *corder = reinterpret_cast<int *>(tb + TL::corder);
   int *crow = reinterpret_cast<int *>(tb + TL::crow);
   int *meta = reinterpret_cast<int *>(tb + TL::meta);
   const bool real = lane < N;
@@ -146,6 +147,16 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
     }
   }
   const int e1 = s1 - dl, e2 = s2 - (lane < N ? dl + 1 : 0);  // exclusive prefix
+  // conv order: nodes whose window lies inside the tree (depth >= K-1) first
+  const bool inside = lane < N && dl >= K - 1;
+  const unsigned lt = (1u << lane) - 1u;
+  const unsigned insm = __ballot_sync(FULL, inside);
+  const unsigned outm = __ballot_sync(FULL, lane < N && !inside);
+  const int n_inside = __popc(insm);
+  if (lane < N)
+    corder[inside ? __popc(insm & lt) : n_inside + __popc(outm & lt)] = lane;
+  else if (lane < NMAX)
+    corder[lane] = 0;
   if (lane <= NMAX) {
     off[lane] = e1;
     off2[lane] = e2;
@@ -154,7 +165,7 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
     meta[0] = P;
     meta[1] = e2;
     meta[2] = e1;
-    meta[3] = 0;
+    meta[3] = n_inside;
   }
   // pairs (node, strict ancestor) and lanes (node, ancestor-or-self)
   {
@@ -211,6 +222,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   const uint32_t stg_bytes =
       (uint32_t)N * kTcD * 2 + (uint32_t)(K - 1) * kTcD * 4 + (uint32_t)kTcD * K * 2;
 
+  // the step kernel may be scheduled as this grid's last CTAs start; it waits
+  // for this grid's completion before it reads the workspace
+  ptx::launch_dependents();
   const int g = blockIdx.x;
   const int kh = g % Hk, lbi = g / Hk;
   const int bq = lbi % Bq, l = lbi / Bq;
@@ -254,7 +268,8 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   const int *n2o = reinterpret_cast<const int *>(tb + TL::n2o);
   const unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn, *ln = tb + TL::ln;
   const int *meta = reinterpret_cast<const int *>(tb + TL::meta);
-  const int P = meta[0], nl = meta[1], npair = meta[2];
+  const int P = meta[0], nl = meta[1], npair = meta[2], n_inside = meta[3];
+  const int *corder = reinterpret_cast<const int *>(tb + TL::corder);
   if (!ptx::mbar_wait(bar, 0)) {
     if (A.status) *A.status = LBX_ETIMEOUT;
     (void)ptx::mbar_wait(bar, 0);  // the copies must land before the CTA exits
@@ -274,11 +289,17 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
     conv_weights8<NMAX>(wsl, K, cs, li * 8);
 #pragma unroll
     for (int p = 0; p < U; ++p) {
+      // units in conv order; a warp holds two nodes and takes the
+      // inputs-only path when both windows lie inside the tree
       const int u = p * NT + tid;
       const bool act = u < N * GQ;
-      const int i = act ? u / GQ : 0;
+      const int slot = u / GQ;
+      const int i = act ? corder[slot] : 0;
       float v8[8];
-      conv8_staged<NMAX>(v8, win + i * 4, wsl, cs, li * 8);
+      if (__all_sync(0xffffffffu, act && slot < n_inside))
+        conv8_staged_tree<NMAX>(v8, win + i * 4, wsl, cs, li * 8);
+      else
+        conv8_staged<NMAX>(v8, win + i * 4, wsl, cs, li * 8);
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
@@ -300,7 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
             make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, li * 8)) =
             make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        float4 *kd = reinterpret_cast<float4 *>(kqf + brow * kTcD + li * 8);
+        float4 *kd = reinterpret_cast<float4 *>(kqf + brow * PL::KQP + li * 8);
         kd[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
         kd[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
       }
@@ -350,9 +371,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int k = 4 * (sub + 8 * c);
-        const float4 kj = *reinterpret_cast<const float4 *>(kqf + j * kTcD + k);
-        const float4 kn = *reinterpret_cast<const float4 *>(kqf + n * kTcD + k);
-        const float4 qn = *reinterpret_cast<const float4 *>(kqf + (NMAX + n) * kTcD + k);
+        const float4 kj = *reinterpret_cast<const float4 *>(kqf + j * PL::KQP + k);
+        const float4 kn = *reinterpret_cast<const float4 *>(kqf + n * PL::KQP + k);
+        const float4 qn = *reinterpret_cast<const float4 *>(kqf + (NMAX + n) * PL::KQP + k);
         s1 += dot4(kj, kn);
         s2 += dot4(kj, qn);
       }

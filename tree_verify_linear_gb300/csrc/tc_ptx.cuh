@@ -91,6 +91,17 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Let the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled once every CTA of this grid has executed this.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid has completed and its memory is visible.
+__device__ __forceinline__ void wait_prerequisite_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- named barrier for a subset of warps -----------------------------------
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
