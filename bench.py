@@ -41,11 +41,15 @@ UNIT = "node-head updates/s"
 
 def step_kernels(w):
     """The kernels one lbx_verify_step call launches for this workload (the
-    library's own selection rule): the tensor-core step (tree mode, d = 128,
-    N <= 24) is a prep kernel per key head followed by the step kernel; the
-    other configurations run one CUDA-core kernel."""
+    library's own selection rule, default mode): tree mode (N <= 64) with
+    d = 128 and N <= 24 is a prep kernel per key head followed by the
+    tensor-core step kernel; chunked mode (longer chains) with d = 128 is the
+    tensor-core chain kernel; the other configurations run one CUDA-core
+    kernel."""
     if w.d == 128 and w.N <= 24:
         return ("gdn_qk_prep_kernel", "gdn_step_tc_kernel")
+    if w.d == 128 and w.N > 64:
+        return ("gdn_chain_tc_kernel",)
     return ("gdn_step_kernel",)
 
 

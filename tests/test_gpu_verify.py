@@ -141,8 +141,14 @@ def test_tree_and_chunked_modes_agree_on_a_chain():
     o1, s1, c1, st1, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
     o2, s2, c2, st2, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
     assert st1 == st2 == 0
-    assert np.abs(o1 - o2).max() <= 1e-5 * np.abs(o1).max()
+    # chunked mode at d = 128 runs on tensor cores (bf16 hi/lo products),
+    # tree mode at N = 64 on CUDA cores (fp32): the same bound as for the
+    # two tree kernels
+    assert np.abs(o1 - o2).max() <= 1e-4 * np.abs(o1).max()
     assert c1.tobytes() == c2.tobytes()
+    used = inp["slot"]  # the other slots hold the canary pattern
+    rel = np.linalg.norm((s1 - s2)[:, used].reshape(-1)) / np.linalg.norm(s1[:, used].reshape(-1))
+    assert rel <= 1e-5
 
 
 def test_identity_gates_keep_state_and_read_out_S0_q():

@@ -44,6 +44,12 @@ bool step_tc_supported(int d, int N, int chain);
 size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int Hv, int N);
 int launch_step_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st);
 
+// Tensor-core chunked step for chains (d = 128): one CTA per (layer,
+// request, value head) sequence, 16-token chunks, arrival counters in the
+// workspace as for the CUDA-core kernels.
+bool chain_tc_supported(int d);
+int launch_chain_tc(const StepArgs &A, cudaStream_t st);
+
 // Workspace of the CUDA-core fused step: one arrival counter per (layer,
 // request, key head), 256-byte rounded.
 size_t counters_bytes(int L, int Bq, int Hk);

@@ -10,6 +10,7 @@
 #include "gdn_launch.h"
 #include "gdn_tc.cuh"
 #include "gdn_tc_prep.cuh"
+#include "gdn_chain_tc.cuh"
 
 namespace lbx {
 namespace {
@@ -116,7 +117,50 @@ int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
 
+int launch_chain(const StepArgs &A, cudaStream_t st) {
+  if (!have_encode()) return LBX_ECUDA;
+  const int nsm = sm_count();
+  if (nsm <= 0) return LBX_ECUDA;
+  const int C = (2 * A.Hk + A.Hv) * kTcD;
+  ChainMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (!encode_2d(&maps.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A.state_in, kTcD,
+                 (uint64_t)A.L * A.n_slots * A.Hv * kTcD, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return LBX_ECUDA;
+  // x as [L * Bq * N rows][C bf16]: one box = one 128-channel block of a
+  // chunk's tokens and the 3 before it
+  if (!encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, A.x, C, (uint64_t)A.L * A.Bq * A.N,
+                 kTcD, kChainRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return LBX_ECUDA;
+  if (A.K > 1 && !encode_2d(&maps.cache, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A.conv_cache, C,
+                            (uint64_t)A.L * A.n_slots * (A.K - 1), kTcD, A.K - 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+    return LBX_ECUDA;
+  ChainArgs T;
+  T.s = A;
+  T.n_seq = A.L * A.Bq * A.Hv;
+  constexpr int smem = ChainLayout::total;
+  if (cudaFuncSetAttribute(gdn_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return LBX_ECUDA;
+  if (cudaFuncSetAttribute(gdn_chain_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return LBX_ECUDA;
+  const int slots = kTcCtasPerSm * nsm;
+  const int grid = T.n_seq < slots ? T.n_seq : slots;
+  gdn_chain_tc_kernel<<<grid, kTcThreads, smem, st>>>(maps, T);
+  return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
+}
+
 }  // namespace
+
+bool chain_tc_supported(int d) { return d == kTcD; }
+
+int launch_chain_tc(const StepArgs &A, cudaStream_t st) {
+  if ((long long)A.L * A.n_slots * A.Hv * kTcD > 0x7fffffffLL) return LBX_EINVAL;
+  if ((long long)A.L * A.Bq * A.N > 0x7fffffffLL) return LBX_EINVAL;
+  return launch_chain(A, st);
+}
 
 bool step_tc_supported(int d, int N, int chain) {
   return d == kTcD && !chain && N >= 1 && N <= 24;

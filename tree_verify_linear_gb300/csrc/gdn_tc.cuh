@@ -315,14 +315,13 @@ __device__ __forceinline__ void conv_weights8(float (&wsl)[8][LBX_MAX_CONV_WIDTH
 // choice between the node row and the cache row is a select, so the unrolled
 // body has no branches.
 template <int NMAX>
-__device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win,
+__device__ __forceinline__ void conv8_staged(float (&out)[8], const int4 w4,
                                              const float (&wsl)[8][LBX_MAX_CONV_WIDTH],
                                              const unsigned char *cs, int c0) {
   using CS = ConvStage<NMAX>;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  const int4 w4 = *reinterpret_cast<const int4 *>(win);
   const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
   for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
@@ -344,14 +343,13 @@ __device__ __forceinline__ void conv8_staged(float (&out)[8], const int *win,
 // conv8_staged for a node whose window lies inside the tree (every row
 // >= 0): no cached-row loads, no selects.
 template <int NMAX>
-__device__ __forceinline__ void conv8_staged_tree(float (&out)[8], const int *win,
+__device__ __forceinline__ void conv8_staged_tree(float (&out)[8], const int4 w4,
                                                   const float (&wsl)[8][LBX_MAX_CONV_WIDTH],
                                                   const unsigned char *cs, int c0) {
   using CS = ConvStage<NMAX>;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  const int4 w4 = *reinterpret_cast<const int4 *>(win);
   const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
   for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {

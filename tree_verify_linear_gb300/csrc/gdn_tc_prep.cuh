@@ -297,9 +297,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       const int i = act ? corder[slot] : 0;
       float v8[8];
       if (__all_sync(0xffffffffu, act && slot < n_inside))
-        conv8_staged_tree<NMAX>(v8, win + i * 4, wsl, cs, li * 8);
+        conv8_staged_tree<NMAX>(v8, *reinterpret_cast<const int4 *>(win + i * 4), wsl, cs, li * 8);
       else
-        conv8_staged<NMAX>(v8, win + i * 4, wsl, cs, li * 8);
+        conv8_staged<NMAX>(v8, *reinterpret_cast<const int4 *>(win + i * 4), wsl, cs, li * 8);
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);

@@ -163,6 +163,7 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
   A.state_in = state, A.state_out = state, A.conv_cache_out = conv_cache;
   A.o = o, A.counters = static_cast<unsigned int *>(workspace), A.status = d_status;
   if (uses_tc(cfg)) return lbx::launch_step_tc(A, workspace, workspace_bytes, stream);
+  if (A.chain && lbx::chain_tc_supported(cfg->d)) return lbx::launch_chain_tc(A, stream);
   return lbx::launch_step_fused(A, cfg->d, stream);
 }
 
