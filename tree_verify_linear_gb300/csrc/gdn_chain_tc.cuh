@@ -55,9 +55,9 @@ struct ChainLayout {
   static constexpr int gam = bn + 4 * kChainC;             // gamma of the previous token
   static constexpr int cpa = gam + 4 * kChainC;            // coefficients g(j -> chunk end)
   static constexpr int cac = cpa + 4 * kChainC;            // coefficients g(j -> accepted)
-  static constexpr int twv = cac + 4 * kChainC;            // float [2][kNLane] T, W lanes
-  static constexpr int lofs = twv + 8 * kNLane;            // uint16 [kNLane]
-  static constexpr int misc = round_up(lofs + 2 * kNLane, 16);
+  static constexpr int lm = cac + 4 * kChainC;             // float [C][C] diag(b a) M
+  static constexpr int qm = lm + 4 * kChainC * kChainC;    // float [C][C] Q
+  static constexpr int misc = qm + 4 * kChainC * kChainC;
   static constexpr int bars = (misc + 64 + 7) & ~7;        // 7 x uint64
   static constexpr int total = bars + 7 * 8;
   static_assert(total <= kTcMaxSmem, "two CTAs per SM");
@@ -118,9 +118,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   float *gam = reinterpret_cast<float *>(smem + CL::gam);
   float *cpa = reinterpret_cast<float *>(smem + CL::cpa);
   float *cac = reinterpret_cast<float *>(smem + CL::cac);
-  uint16_t *lofs = reinterpret_cast<uint16_t *>(smem + CL::lofs);
+  float *Lm = reinterpret_cast<float *>(smem + CL::lm);
+  float *Qm = reinterpret_cast<float *>(smem + CL::qm);
   int *misc = reinterpret_cast<int *>(smem + CL::misc);
-  // misc[0] error flag, [1] abort, [2] last arriver, [3] TMEM base
+  // misc[0] error flag, [2] last arriver, [3] TMEM base
   float *fmisc = reinterpret_cast<float *>(misc + 8);  // [0] gamma_end, [1] gamma_acc
   uint64_t *stage_bar = reinterpret_cast<uint64_t *>(smem + CL::bars);
   uint64_t *qk_bar = stage_bar + 1;
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
   }
   if (tid == 0) {
-    misc[1] = 0;
     ptx::mbar_init(stage_bar, 1);
     ptx::mbar_init(qk_bar, 1);
     ptx::mbar_init(v_bar, 1);
@@ -159,13 +159,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
   }
-  // chain tables: lane q = n (n + 1) / 2 + L is (node n, node n - L); its T
-  // entry sits at lofs[q] in the [T|W] operand; entries off the lanes stay 0
-  for (int q = tid; q < CL::kNLane; q += kTcThreads) {
-    int n = 0;
-    while ((n + 1) * (n + 2) / 2 <= q) ++n;
-    lofs[q] = (uint16_t)plain_bf16(KP, n, n - (q - n * (n + 1) / 2));
-  }
+  // entries of [T|W] above the diagonal stay 0
   for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
     *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
@@ -178,10 +172,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 
   uint32_t stage_waits = 0, qk_waits = 0, v_waits = 0, mma_waits = 0;
   int n_stage = 0, n_qk = 0, n_v = 0;
+  // a wait that timed out in this thread (bad); the block's decision to stop
+  // (aborted), taken at a barrier reduction so that every thread agrees
+  bool bad = false, aborted = false;
   auto wait_on = [&](uint64_t *bar, uint32_t &waits) {
     if (!ptx::mbar_wait(bar, waits & 1u)) {
       if (A.status) *A.status = LBX_ETIMEOUT;
-      atomicExch(&misc[1], 1);
+      bad = true;
     }
     ++waits;
   };
@@ -291,112 +288,149 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         }
       }
 
-      // ---- Gram entries from the operand (hi + lo), 8 threads per item:
-      // pairs (n, j < n) at e = n(n-1)/2 + (n-1-j), then the diagonals ----
-      {
-        constexpr int items = CL::kNPair + C;
-        const int sub = tid & 7;
-        for (int base = 0; base < items; base += kTcThreads / 8) {
-          const int item = base + (tid >> 3);
-          const bool act = item < items;
-          int j = 0, n = 0;
-          if (act) {
-            if (item < CL::kNPair) {
-              n = 1;
-              while ((n + 1) * n / 2 <= item) ++n;
-              j = n - 1 - (item - n * (n - 1) / 2);
-            } else {
-              j = n = item - CL::kNPair;
-            }
-          }
-          float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int k = 8 * (sub + 8 * c);
-            float kj[8], kn[8], qn[8];
-            image_row8(B1, R1, NC, j, k, kj);
-            image_row8(B1, R1, NC, n, k, kn);
-            image_row8(B1, R1, NC, NMAX + n, k, qn);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              s1 = fmaf(kj[e], kn[e], s1);
-              s2 = fmaf(kj[e], qn[e], s2);
-            }
-          }
-#pragma unroll
-          for (int o = 4; o > 0; o >>= 1) {
-            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-          }
-          if (act && sub == 0) {
-            if (item < CL::kNPair) {
-              gkk[item] = s1;
-              gkq[item] = s2;
-            } else {
-              kqn[n] = s2;
-            }
-          }
-        }
-      }
-      // ---- gate products: gamma of the previous token, coefficients to the
-      // chunk's last token and to the accepted token ----
+      // ---- Gram matrix K [K|Q]^T on the tensor cores: the product MMA1
+      // forms with S0, taken with the operand's first 32 rows (K, then Q) as
+      // A.  Warps 0 and 4 (TMEM lanes 0..31) copy those rows, hi and lo, into
+      // the S0 columns, free until the split; lanes 32..127 of A and of the
+      // product are not used.  Warp 1 meanwhile forms the gate products: gamma
+      // of the previous token, coefficients to the chunk's last token and to
+      // the accepted token ----
       const bool acc_here = ch == ch_acc;
       const int acc_l = acc - t0;
-      if (tid < C) {
-        float g = 1.f;
-        for (int u = 0; u < tid; ++u) g *= an[u];
-        gam[tid] = g;
-        float c = tid < nc ? 1.f : 0.f;
-        for (int u = tid + 1; u < nc; ++u) c *= an[u];
-        cpa[tid] = c;
-        float ca = acc_here && tid <= acc_l ? 1.f : 0.f;
-        for (int u = tid + 1; u <= acc_l && u < C; ++u) ca *= an[u];
-        cac[tid] = ca;
-        if (tid == 0) {
-          float ge = 1.f, ga = 1.f;
-          for (int u = 0; u < nc; ++u) ge *= an[u];
-          for (int u = 0; u <= acc_l && u < C; ++u) ga *= an[u];
-          fmisc[0] = ge;
-          fmisc[1] = ga;
+      if (warp == 0 || warp == 4) {
+        const int lo = warp >> 2, row = lo * NC + (tid & 31);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 u =
+                *reinterpret_cast<const uint4 *>(B1 + sw128_bf16(R1, row, 64 * c + 8 * q));
+            v[4 * q] = u.x;
+            v[4 * q + 1] = u.y;
+            v[4 * q + 2] = u.z;
+            v[4 * q + 3] = u.w;
+          }
+          ptx::tmem_st32(tq + Ly::cA1 + 64 * lo + 32 * c, v);
+        }
+        ptx::tmem_wait_st();
+      } else if (warp == 1) {
+        // prefix and suffix products of the gates over the chunk's tokens
+        const int lane = tid & 31;
+        const float a = lane < C ? an[lane] : 1.f;
+        float pre = a;  // a_0 ... a_lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, pre, o);
+          if (lane >= o) pre *= t;
+        }
+        const float pre_ex = __shfl_up_sync(0xffffffffu, pre, 1);
+        auto suffix_from = [&](int end) {  // product of a_(lane+1) .. a_(end-1)
+          float suf = lane < end ? a : 1.f;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 32) suf *= t;
+          }
+          const float ex = __shfl_down_sync(0xffffffffu, suf, 1);
+          return lane + 1 < 32 ? ex : 1.f;
+        };
+        const float c_end = suffix_from(nc);
+        const float c_acc = suffix_from(acc_here ? acc_l + 1 : 0);
+        const float g_end = __shfl_sync(0xffffffffu, pre, nc - 1);
+        const float g_acc = __shfl_sync(0xffffffffu, pre, acc_here ? acc_l : 0);
+        if (lane < C) {
+          gam[lane] = lane == 0 ? 1.f : pre_ex;
+          cpa[lane] = lane < nc ? c_end : 0.f;
+          cac[lane] = acc_here && lane <= acc_l ? c_acc : 0.f;
+        }
+        if (lane == 0) {
+          fmisc[0] = g_end;
+          fmisc[1] = g_acc;
         }
       }
+      ptx::tc_fence_before();
+      __syncthreads();
+      if (lead) {
+        ptx::tc_fence_after();
+        mma_kq<NMAX>(tmem + Ly::cD1, tmem + Ly::cA1, ptx::smem_u32(B1));
+        ptx::mma_commit(mma_bar);
+      }
+      wait_on(mma_bar, mma_waits);
+      ptx::tc_fence_after();
+      if (warp == 0) {
+        // lane j < C: k_j.[k_n | q_n] = column n + column n + NC
+        float g0[32], g1[32];
+        ptx::tmem_ld32(tq + Ly::cD1, g0);
+        ptx::tmem_ld32(tq + Ly::cD1 + 32, g1);
+        ptx::tmem_wait_ld();
+        const int jr = tid;
+        if (jr < C) {
+#pragma unroll
+          for (int n = 0; n < C; ++n) {
+            const float kk = g0[n] + g1[n], kq = g0[NMAX + n] + g1[NMAX + n];
+            if (n > jr) {
+              const int e = n * (n - 1) / 2 + (n - 1 - jr);
+              gkk[e] = kk;
+              gkq[e] = kq;
+            }
+            if (n == jr) kqn[n] = kq;
+          }
+        }
+      }
+      ptx::tc_fence_before();
       __syncthreads();
 
-      // ---- T and W lanes: lane q = (node n, node m = n - L); the stretch
-      // m -> n of the chain is m, m+1, ..., n ----
-      for (int q = tid; q < CL::kNLane; q += kTcThreads) {
-        int n = 0;
-        while ((n + 1) * (n + 2) / 2 <= q) ++n;
-        const int L = q - n * (n + 1) / 2, m = n - L;
-        Tf[m * TP + m] = 1.f;
-        float xl = 1.f;
-        for (int p = 1; p <= L; ++p) {
-          const int jp = m + p, ep = jp * (jp - 1) / 2 + jp - 1;  // pair (jp, jq): ep - jq
-          float sacc = 0.f, g = 1.f;
-          for (int qq = p - 1; qq >= 0; --qq) {
-            const int jq = m + qq;
-            sacc = fmaf(g * gkk[ep - jq], Tf[jq * TP + m], sacc);
-            g *= an[jq];
-          }
-          xl = -bn[jp] * an[jp] * sacc;
-          Tf[jp * TP + m] = xl;
+      // ---- T = (I + L)^-1 with L = diag(b a) M, and W = Q T, for the
+      // chunk's chain: L[n][j] = b_n a_n g(j->n-1) k_j.k_n, Q[n][j] =
+      // a_n g(j->n-1) k_j.q_n (j < n), Q[n][n] = k_n.q_n ----
+      {
+        const int n = tid >> 4, j = tid & 15;  // entry (n, j), C * C = 256 threads
+        float lv = 0.f, qv = j == n ? kqn[n] : 0.f;
+        if (j < n) {
+          float g = 1.f;
+          for (int u = j + 1; u < n; ++u) g *= an[u];
+          const int e = n * (n - 1) / 2 + (n - 1 - j);
+          lv = bn[n] * an[n] * g * gkk[e];
+          qv = an[n] * g * gkq[e];
         }
-        float sacc = 0.f, g = 1.f;
-        const int en = n * (n - 1) / 2 + n - 1;
-        for (int qq = L - 1; qq >= 0; --qq) {
-          const int jq = m + qq;
-          sacc = fmaf(g * gkq[en - jq], Tf[jq * TP + m], sacc);
-          g *= an[jq];
+        Lm[n * C + j] = lv;
+        Qm[n * C + j] = qv;
+      }
+      __syncthreads();
+      {
+        // column m of T on half-warp m: row n of (I + L) T = I gives
+        // T[n][m] = [n == m] - sum_{j<n} L[n][j] T[j][m]; lane j keeps T[j][m]
+        const int m = tid >> 4, jj = tid & 15;
+        float tcol = jj == m ? 1.f : 0.f;
+#pragma unroll
+        for (int n = 1; n < C; ++n) {
+          float t = jj < n ? Lm[n * C + jj] * tcol : 0.f;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          const float val = (n == m ? 1.f : 0.f) - t;
+          if (jj == n) tcol = val;
         }
-        const float wv = fmaf(kqn[n], xl, an[n] * sacc);
-        uint16_t th, tl, wh, wl;
-        split_bf16(xl, th, tl);
-        split_bf16(wv, wh, wl);
-        const uint32_t o = lofs[q];
-        *reinterpret_cast<uint16_t *>(B2hi + o) = th;
-        *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
-        *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
-        *reinterpret_cast<uint16_t *>(B2lo + o + Ly::kWOff) = wl;
+        Tf[jj * TP + m] = tcol;
+      }
+      __syncthreads();
+      {
+        // W[n][m] = sum_j Q[n][j] T[j][m]; T and W entries (n >= m) -> [T|W]
+        const int n = tid >> 4, m = tid & 15;
+        if (m <= n) {
+          float wv = 0.f;
+#pragma unroll
+          for (int j = 0; j < C; ++j) wv = fmaf(Qm[n * C + j], Tf[j * TP + m], wv);
+          const float tv = Tf[n * TP + m];
+          uint16_t th, tl, wh, wl;
+          split_bf16(tv, th, tl);
+          split_bf16(wv, wh, wl);
+          const uint32_t o = plain_bf16(KP, n, m);
+          *reinterpret_cast<uint16_t *>(B2hi + o) = th;
+          *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
+          *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
+          *reinterpret_cast<uint16_t *>(B2lo + o + Ly::kWOff) = wl;
+        }
       }
       ptx::fence_proxy_async();
 
@@ -416,8 +450,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      __syncthreads();  // ------------------------------------------------ S1
-      if (misc[1]) break;
+      if (__syncthreads_or(bad)) {  // ------------------------------------------------ S1
+        aborted = true;
+        break;
+      }
       if (lead) {
         ptx::tc_fence_after();
         mma_kq<NMAX>(tmem + Ly::cD1, tmem + Ly::cA1, ptx::smem_u32(B1));
@@ -484,8 +520,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         rhs_half(std::integral_constant<int, 1>{});
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      __syncthreads();  // ------------------------------------------------ S2
-      if (misc[1]) break;
+      if (__syncthreads_or(bad)) {  // ------------------------------------------------ S2
+        aborted = true;
+        break;
+      }
       if (lead) {
         // MMA2: [delta | W rhs] = rhs [T|W]^T, three passes over K = KP
         ptx::tc_fence_after();
@@ -596,7 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       if (ch + 1 < nch || end_is_acc) state_pass(cpa, fmisc[0], end_is_acc, ch + 1 < nch);
       __syncthreads();  // the chunk's shared data is free
     }
-    if (misc[1]) break;
+    if (aborted) break;
 
     // ---- new conv window of the slot: the K-1 raw inputs ending at the
     // accepted token (continuing into the old window); v channels of this
@@ -619,7 +657,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   }
 
   // ---- drain: copies still in flight after an abort ----
-  if (lead && misc[1]) {
+  if (lead && aborted) {
     if (n_stage > 0) (void)ptx::mbar_wait(stage_bar, (uint32_t)((n_stage - 1) & 1));
     if (n_qk > 0) (void)ptx::mbar_wait(qk_bar, (uint32_t)((n_qk - 1) & 1));
     if (n_v > 0) (void)ptx::mbar_wait(v_bar, (uint32_t)((n_v - 1) & 1));

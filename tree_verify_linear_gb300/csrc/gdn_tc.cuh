@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   const float *gam = reinterpret_cast<const float *>(hr + HL::gam);
   const float *cpa = reinterpret_cast<const float *>(hr + HL::cpa);
   int *misc = reinterpret_cast<int *>(smem + Ly::misc);
-  // misc[0] error flag, [1] abort, [3] TMEM base
+  // misc[0] error flag, [3] TMEM base
   uint64_t *stage_bar = reinterpret_cast<uint64_t *>(smem + Ly::bars);
   uint64_t *stg_bar = stage_bar + 1;
   uint64_t *mma_bar = stage_bar + 2;
@@ -492,7 +492,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 
   // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
-    misc[1] = 0;
     ptx::mbar_init(stage_bar, 1);
     ptx::mbar_init(stg_bar, 1);
     ptx::mbar_init(mma_bar, 1);
@@ -597,10 +596,13 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   };
   // phases waited for, the same count in every thread
   uint32_t stg_waits = 0, mma_waits = 0, rec_waits = 0, tab_waits = 0, hr_waits = 0;
+  // a wait that timed out in this thread (bad); the block's decision to stop
+  // (aborted), taken at a barrier reduction so that every thread agrees
+  bool bad = false, aborted = false;
   auto wait_on = [&](uint64_t *bar, uint32_t &waits) {
     if (!ptx::mbar_wait(bar, waits & 1u)) {
       if (A.status) *A.status = LBX_ETIMEOUT;
-      atomicExch(&misc[1], 1);
+      bad = true;
     }
     ++waits;
   };
@@ -673,7 +675,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     // ================= S0 -> tensor memory (bf16 hi / lo) =================
     if (!ptx::mbar_wait(stage_bar, (uint32_t)(it & 1))) {
       if (A.status) *A.status = LBX_ETIMEOUT;
-      atomicExch(&misc[1], 1);
+      bad = true;
     }
     {
       // this thread's 64 columns of the row: hi into A columns hf*32.., lo
@@ -691,8 +693,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
-    __syncthreads();  // ---------------------------------------------- S1
-    if (misc[1]) break;
+    if (__syncthreads_or(bad)) {  // ---------------------------------------------- S1
+      aborted = true;
+      break;
+    }
 
     if (lead) {
       // MMA1: [S0 k | S0 q] = S0 [K|Q]^T over K = 128
@@ -792,8 +796,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
-    __syncthreads();  // ---------------------------------------------- S2
-    if (misc[1]) break;
+    if (__syncthreads_or(bad)) {  // ---------------------------------------------- S2
+      aborted = true;
+      break;
+    }
     if (lead && it + 1 < count) load_state(nx);  // the stage has been read
     if (lead) {
       // MMA2: [delta | W rhs] = rhs [T|W]^T, three passes over K = KP
@@ -846,8 +852,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       od_half(std::integral_constant<int, 1>{});
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
-    __syncthreads();  // ---------------------------------------------- S3
-    if (misc[1]) break;
+    if (__syncthreads_or(bad)) {  // ---------------------------------------------- S3
+      aborted = true;
+      break;
+    }
     if (lead) {
       // MMA3: sum_j c_j delta_j k_j^T over the path rows of operand K,
       // read N-major, three passes over K = KP
@@ -898,13 +906,15 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       }
     }
     ptx::tc_fence_before();
-    __syncthreads();  // ---------------------------------------------- S4
-    if (misc[1]) break;
+    if (__syncthreads_or(bad)) {  // ---------------------------------------------- S4
+      aborted = true;
+      break;
+    }
     if (lead && it + 1 < count && nx.bq != bq) load_tab(nx);
   }
 
   // ---- drain: copies still in flight after an abort ----
-  if (lead && misc[1]) {
+  if (lead && aborted) {
     if (n_state_loads > 0) (void)ptx::mbar_wait(stage_bar, (uint32_t)((n_state_loads - 1) & 1));
     if (n_stg_loads > 0) (void)ptx::mbar_wait(stg_bar, (uint32_t)((n_stg_loads - 1) & 1));
     if (n_rec_loads > 0) (void)ptx::mbar_wait(rec_bar, (uint32_t)((n_rec_loads - 1) & 1));

@@ -9,9 +9,17 @@
 namespace lbx {
 namespace ptx {
 
-// Upper bound on polls of one mbarrier before a kernel gives up and reports
-// LBX_ETIMEOUT (each poll may also suspend the thread for a short time).
+// Upper bound on the time one mbarrier wait may take before a kernel gives up
+// and reports LBX_ETIMEOUT: one second of the global nanosecond timer.  A
+// poll count caps the loop as well, in case the timer does not advance.
+constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -41,10 +49,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Returns false if the phase did not complete within kWaitLimit polls.
+// Returns false if the phase did not complete within kWaitNs (or kWaitLimit
+// polls); the timer is read only once the first poll has failed.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitNs) return false;
+  }
   return false;
 }
 
