@@ -90,18 +90,25 @@ __device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.0f 
 //   chain:          every parent array must be the chain parent[i] == i-1
 //   check_accepted: accepted[b] in [0, N)
 //   check_distinct: no two requests name the same slot
+// The checks are spread over the threads first, first + stride, ... (the
+// whole block by default).
 __device__ __forceinline__ int validate_batch(const int32_t *parent, const int32_t *slot,
                                               const int32_t *accepted, int Bq, int N,
                                               int n_slots, bool chain, bool check_accepted,
-                                              bool check_distinct) {
+                                              bool check_distinct, int first = -1,
+                                              int stride = 0) {
+  if (first < 0) {
+    first = threadIdx.x;
+    stride = blockDim.x;
+  }
   int bad = 0;
-  for (int idx = threadIdx.x; idx < Bq * N; idx += blockDim.x) {
+  for (int idx = first; idx < Bq * N; idx += stride) {
     int i = idx % N;
     int p = parent[idx];
     bool ok = chain ? (p == i - 1) : (i == 0 ? p == -1 : (p >= 0 && p < i));
     if (!ok) bad = LBX_ETREE;
   }
-  for (int b = threadIdx.x; b < Bq; b += blockDim.x) {
+  for (int b = first; b < Bq; b += stride) {
     int s = slot[b];
     if (s < 0 || s >= n_slots) bad = LBX_EINVAL;
     if (check_accepted) {

@@ -800,7 +800,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       aborted = true;
       break;
     }
-    if (lead && it + 1 < count) load_state(nx);  // the stage has been read
     if (lead) {
       // MMA2: [delta | W rhs] = rhs [T|W]^T, three passes over K = KP
       ptx::tc_fence_after();
@@ -820,6 +819,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
         }
       }
       ptx::mma_commit(mma_bar);
+      if (it + 1 < count) load_state(nx);  // the stage has been read
     }
 
     // ================= o, path deltas -> tensor memory =================

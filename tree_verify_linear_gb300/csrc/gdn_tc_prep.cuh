@@ -6,7 +6,8 @@
 //     path (q scaled), written to the workspace as the bf16 hi / lo [K|Q]
 //     operand image of the step kernel;
 //   * the Gram entries k_j.k_n, k_j.q_n of every (node n, strict ancestor j)
-//     pair and k_n.q_n, from the same hi + lo values the tensor cores see;
+//     pair and k_n.q_n, in fp32 (the tensor cores see hi + lo, within
+//     2^-17 of the same values);
 //   * for each value head of the key head: its gates in the new labels, the
 //     entries of T = (I + diag(b a) M)^-1 and W = Q T on every (node,
 //     ancestor-or-self) lane, gamma of each node's parent, the accepted-path
@@ -226,10 +227,12 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   // for this grid's completion before it reads the workspace
   ptx::launch_dependents();
   const int g = blockIdx.x;
+  unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
+  int *porig = reinterpret_cast<int *>(smem + PL::porig);
+  const int warp = tid >> 5;
   const int kh = g % Hk, lbi = g / Hk;
   const int bq = lbi % Bq, l = lbi / Bq;
   unsigned char *img = T.ws + tc_tab_bytes<NMAX>(Bq) + (size_t)g * Ly::kB;
-  unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
 
   // The copies only read, so they start before the batch is validated (an
   // out-of-range slot is clamped here; such a batch is rejected below).
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   slot_b = slot_b < 0 ? 0 : (slot_b >= A.n_slots ? A.n_slots - 1 : slot_b);
   if (tid == 0) {
     const int crow0 = (l * A.n_slots + slot_b) * (K - 1);
+    misc[0] = 0;
     ptx::mbar_init(bar, 1);
     ptx::fence_mbar_init();
     ptx::mbar_arrive_expect_tx(bar, 2 * stg_bytes);
@@ -249,91 +253,136 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
                      (uint32_t)kTcD * K * 2, bar);
     }
   }
-  // tables (warp 0) while the copies fly; an invalid batch is reported by
-  // the step kernel, and nothing is written here
-  if (tid < 32) build_tables_warp<NMAX>(tid, N, K, A.accepted[bq], A.parent + (size_t)bq * N, tb);
-  {
-    const int code =
-        validate_batch(A.parent, A.slot, A.accepted, Bq, N, A.n_slots, false, true, true);
-    if (block_any_error(code, misc)) {
-      if (tid == 0) (void)ptx::mbar_wait(bar, 0);  // the copies land before the CTA exits
-      return;
+  // input parents (clamped to the tree rules, so that every window row is a
+  // valid index even for a batch rejected below) and the first value heads'
+  // gates, in input labels, while the copies fly
+  if (tid < NMAX) {
+    int p = tid < N ? A.parent[(size_t)bq * N + tid] : -1;
+    if (!(p >= 0 && p < tid)) p = -1;
+    porig[tid] = p;
+  }
+  const int nh0 = G < kPrepHeads ? G : kPrepHeads;
+  float ga0 = 0.f, gb0 = 0.f;
+  if (tid < kPrepHeads * NP) {
+    const int hh = tid / NP, o = tid % NP;
+    if (hh < nh0 && o < N) {
+      const size_t gi = ((size_t)lbi * N + o) * Hv + kh * G + hh;
+      ga0 = bf2f(A.a[gi]);
+      gb0 = bf2f(A.b[gi]);
     }
   }
-  const int *win = reinterpret_cast<const int *>(tb + TL::win);
+  __syncthreads();
+
+  // Warp 0 builds the request's tree tables and checks the batch while warps
+  // 1..7 run the q, then k conv + SiLU + L2 norm of every node (input
+  // labels, windows walked along the parents) into fp32 rows.
+  int code = 0;
+  if (warp == 0) {
+    build_tables_warp<NMAX>(tid, N, K, A.accepted[bq], A.parent + (size_t)bq * N, tb);
+    code = validate_batch(A.parent, A.slot, A.accepted, Bq, N, A.n_slots, false, true, true,
+                          tid, 32);
+  } else if (!ptx::mbar_wait(bar, 0)) {
+    code = LBX_ETIMEOUT;
+  } else {
+    constexpr int CT = kPrepThreads - 32;  // conv threads
+    constexpr int GQ = kTcD / 8;           // 16 threads per node, 8 channels each
+    constexpr int U = (NMAX * GQ + CT - 1) / CT;
+    static_assert(CT % GQ == 0, "channel group fixed per thread");
+    const int ct = tid - 32, li = ct % GQ;
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      const unsigned char *cs = which == 0 ? sq : sk;
+      float wsl[8][LBX_MAX_CONV_WIDTH];
+      conv_weights8<NMAX>(wsl, K, cs, li * 8);
+#pragma unroll
+      for (int p = 0; p < U; ++p) {
+        const int u = p * CT + ct;
+        const bool act = u < N * GQ;
+        const int o = act ? u / GQ : 0;
+        // window rows: the node, then its ancestors; past the root the
+        // cached rows, newest first (-1 - row); taps j >= K read row 0
+        int wj[4];
+        bool inside = act;
+        {
+          int m = o, past = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            int w = 0;
+            if (j < K) {
+              if (m >= 0) {
+                w = m;
+              } else {
+                ++past;
+                w = -1 - (K - 1 - past);
+                inside = false;
+              }
+            }
+            wj[j] = w;
+            if (j < K && m >= 0) m = porig[m];
+          }
+        }
+        const int4 w4 = make_int4(wj[0], wj[1], wj[2], wj[3]);
+        float v8[8];
+        // a warp holds two nodes; the inputs-only path when both windows
+        // lie inside the tree
+        if (__all_sync(0xffffffffu, inside))
+          conv8_staged_tree<NMAX>(v8, w4, wsl, cs, li * 8);
+        else
+          conv8_staged<NMAX>(v8, w4, wsl, cs, li * 8);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
+#pragma unroll
+        for (int sh = GQ / 2; sh > 0; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+        if (act) {
+          const float scale = rsqrtf(ss + A.l2_eps) * (which == 0 ? A.q_scale : 1.f);
+          float4 *kd = reinterpret_cast<float4 *>(kqf + ((which == 0 ? NMAX : 0) + o) * PL::KQP +
+                                                  li * 8);
+          kd[0] = make_float4(scale * v8[0], scale * v8[1], scale * v8[2], scale * v8[3]);
+          kd[1] = make_float4(scale * v8[4], scale * v8[5], scale * v8[6], scale * v8[7]);
+        }
+      }
+    }
+  }
+  // one barrier: conv rows and tables written, and the block's verdict
+  if (code) atomicExch(&misc[0], code);
+  if (__syncthreads_or(code != 0)) {
+    // an invalid batch is reported by the step kernel; a timeout here
+    if (tid == 0) {
+      if (misc[0] == LBX_ETIMEOUT && A.status) *A.status = LBX_ETIMEOUT;
+      (void)ptx::mbar_wait(bar, 0);  // the copies land before the CTA exits
+    }
+    return;
+  }
   const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
   const int *dep = reinterpret_cast<const int *>(tb + TL::dep);
   const int *off = reinterpret_cast<const int *>(tb + TL::off);
   const int *off2 = reinterpret_cast<const int *>(tb + TL::off2);
   const int *n2o = reinterpret_cast<const int *>(tb + TL::n2o);
+  const int *o2n = reinterpret_cast<const int *>(tb + TL::o2n);
   const unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn, *ln = tb + TL::ln;
   const int *meta = reinterpret_cast<const int *>(tb + TL::meta);
-  const int P = meta[0], nl = meta[1], npair = meta[2], n_inside = meta[3];
-  const int *corder = reinterpret_cast<const int *>(tb + TL::corder);
-  if (!ptx::mbar_wait(bar, 0)) {
-    if (A.status) *A.status = LBX_ETIMEOUT;
-    (void)ptx::mbar_wait(bar, 0);  // the copies must land before the CTA exits
-    return;
-  }
+  const int P = meta[0], nl = meta[1], npair = meta[2];
 
-  // q, then k: conv + SiLU + L2 norm -> operand rows (hi, lo) of the image in
-  // the workspace, and their fp32 values hi + lo for the Gram entries
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    const unsigned char *cs = which == 0 ? sq : sk;
-    constexpr int GQ = kTcD / 8;  // 16 threads per node, the same 8 channels for every node
-    constexpr int U = (NMAX * GQ + NT - 1) / NT;
-    static_assert(NT % GQ == 0, "channel group fixed per thread");
-    const int li = tid % GQ;
-    float wsl[8][LBX_MAX_CONV_WIDTH];
-    conv_weights8<NMAX>(wsl, K, cs, li * 8);
-#pragma unroll
-    for (int p = 0; p < U; ++p) {
-      // units in conv order; a warp holds two nodes and takes the
-      // inputs-only path when both windows lie inside the tree
-      const int u = p * NT + tid;
-      const bool act = u < N * GQ;
-      const int slot = u / GQ;
-      const int i = act ? corder[slot] : 0;
-      float v8[8];
-      if (__all_sync(0xffffffffu, act && slot < n_inside))
-        conv8_staged_tree<NMAX>(v8, *reinterpret_cast<const int4 *>(win + i * 4), wsl, cs, li * 8);
-      else
-        conv8_staged<NMAX>(v8, *reinterpret_cast<const int4 *>(win + i * 4), wsl, cs, li * 8);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(v8[e], v8[e], ss);
-#pragma unroll
-      for (int o = GQ / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (act) {
-        const float scale = rsqrtf(ss + A.l2_eps) * (which == 0 ? A.q_scale : 1.f);
-        const int brow = which == 0 ? NMAX + i : i;
-        uint32_t wh[4], wl[4];
-        float kv[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          split_bf16x2(scale * v8[2 * e], scale * v8[2 * e + 1], wh[e], wl[e]);
-          kv[2 * e] = __uint_as_float(wh[e] << 16) + __uint_as_float(wl[e] << 16);
-          kv[2 * e + 1] =
-              __uint_as_float(wh[e] & 0xffff0000u) + __uint_as_float(wl[e] & 0xffff0000u);
-        }
-        *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, brow, li * 8)) =
-            make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, li * 8)) =
-            make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        float4 *kd = reinterpret_cast<float4 *>(kqf + brow * PL::KQP + li * 8);
-        kd[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
-        kd[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
-      }
+  // operand image in the new labels (K rows, then Q rows; hi rows, then lo
+  // rows NC further): the hi / lo split of the fp32 rows, zero padding rows
+  for (int idx = tid; idx < NC * (kTcD / 8); idx += NT) {
+    const int brow = idx / (kTcD / 8), c8 = idx % (kTcD / 8);
+    const int nlab = brow % NMAX;
+    uint32_t wh[4] = {0u, 0u, 0u, 0u}, wl[4] = {0u, 0u, 0u, 0u};
+    if (nlab < N) {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          kqf + ((brow - nlab) + n2o[nlab]) * PL::KQP + c8 * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      split_bf16x2(x0.x, x0.y, wh[0], wl[0]);
+      split_bf16x2(x0.z, x0.w, wh[1], wl[1]);
+      split_bf16x2(x1.x, x1.y, wh[2], wl[2]);
+      split_bf16x2(x1.z, x1.w, wh[3], wl[3]);
     }
-    // padding rows of this half of the operand are zero
-    for (int idx = tid; idx < (NMAX - N) * 16; idx += NT) {
-      const int brow = (which == 0 ? NMAX : 0) + N + idx / 16;
-      *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, brow, 8 * (idx % 16))) =
-          make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, 8 * (idx % 16))) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
+    *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, brow, c8 * 8)) =
+        make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, c8 * 8)) =
+        make_uint4(wl[0], wl[1], wl[2], wl[3]);
   }
   {
     // new conv window of the key head's q (threads 0..127) and k (128..255)
@@ -349,10 +398,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       cache_o[(size_t)rr * C + gc] = w >= 0 ? bf2f(xs[w * kTcD + c]) : cc[(-1 - w) * kTcD + c];
     }
   }
-  __syncthreads();  // the staged inputs are dead from here on
   {
     // Gram entries, 8 threads per item: the parent-path pairs, then the
-    // diagonals
+    // diagonals (new labels; the fp32 rows are in input labels)
     const int items = npair + N;
     const int sub = tid & 7;
     for (int base = 0; base < items; base += NT / 8) {
@@ -367,13 +415,14 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
           j = n = item - npair;
         }
       }
+      const int jo = n2o[j], no = n2o[n];
       float s1 = 0.f, s2 = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int k = 4 * (sub + 8 * c);
-        const float4 kj = *reinterpret_cast<const float4 *>(kqf + j * PL::KQP + k);
-        const float4 kn = *reinterpret_cast<const float4 *>(kqf + n * PL::KQP + k);
-        const float4 qn = *reinterpret_cast<const float4 *>(kqf + (NMAX + n) * PL::KQP + k);
+        const float4 kj = *reinterpret_cast<const float4 *>(kqf + jo * PL::KQP + k);
+        const float4 kn = *reinterpret_cast<const float4 *>(kqf + no * PL::KQP + k);
+        const float4 qn = *reinterpret_cast<const float4 *>(kqf + (NMAX + no) * PL::KQP + k);
         s1 += dot4(kj, kn);
         s2 += dot4(kj, qn);
       }
@@ -392,24 +441,35 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
     }
   }
-  __syncthreads();
+  __syncthreads();  // the staged inputs are dead from here on
 
   // ---- the G value heads of this key head, kPrepHeads at a time ----
 #pragma unroll 1
   for (int hc = 0; hc < G; hc += kPrepHeads) {
     const int nh = G - hc < kPrepHeads ? G - hc : kPrepHeads;
-    // gates of head hc + hh in the new labels (0 for padding nodes)
-    for (int idx = tid; idx < kPrepHeads * NP; idx += NT) {
-      const int hh = idx / NP, n = idx % NP;
-      float av = 0.f, bv = 0.f;
-      if (hh < nh && n < N) {
-        const size_t gi = ((size_t)lbi * N + n2o[n]) * Hv + kh * G + hc + hh;
-        av = bf2f(A.a[gi]);
-        bv = bf2f(A.b[gi]);
+    // gates of head hc + hh in the new labels (0 for padding nodes); the
+    // first heads' were loaded at the start, in input labels
+    if (hc == 0) {
+      if (tid < kPrepHeads * NP) {
+        const int hh = tid / NP, o = tid % NP;
+        const int nlab = o < N ? o2n[o] : o;
+        han[hh * NP + nlab] = ga0;
+        hbn[hh * NP + nlab] = gb0;
+        hgam[tid] = 0.f;
       }
-      han[idx] = av;
-      hbn[idx] = bv;
-      hgam[idx] = 0.f;
+    } else {
+      for (int idx = tid; idx < kPrepHeads * NP; idx += NT) {
+        const int hh = idx / NP, n = idx % NP;
+        float av = 0.f, bv = 0.f;
+        if (hh < nh && n < N) {
+          const size_t gi = ((size_t)lbi * N + n2o[n]) * Hv + kh * G + hc + hh;
+          av = bf2f(A.a[gi]);
+          bv = bf2f(A.b[gi]);
+        }
+        han[idx] = av;
+        hbn[idx] = bv;
+        hgam[idx] = 0.f;
+      }
     }
     __syncthreads();
     // one task per (head, node n, ancestor-or-self m): column m of T along
