@@ -55,12 +55,18 @@ struct ChainLayout {
   static constexpr int gam = bn + 4 * kChainC;             // gamma of the previous token
   static constexpr int cpa = gam + 4 * kChainC;            // coefficients g(j -> chunk end)
   static constexpr int cac = cpa + 4 * kChainC;            // coefficients g(j -> accepted)
-  static constexpr int lm = cac + 4 * kChainC;             // float [C][C] diag(b a) M
-  static constexpr int qm = lm + 4 * kChainC * kChainC;    // float [C][C] Q
-  static constexpr int misc = qm + 4 * kChainC * kChainC;
+  // float [C][C] matrices of the chunk: L = diag(b a) M, Q, and the scratch
+  // of T = (I + L)^-1 (row-major, some also transposed); tf is one of them
+  static constexpr int kMP = kChainC + 4;                  // padded row pitch (banks)
+  static constexpr int kMat = 4 * kChainC * kMP;
+  static constexpr int lm = cac + 4 * kChainC;
+  static constexpr int qm = lm + kMat;
+  static constexpr int mx = qm + kMat;                     // three more matrices
+  static constexpr int misc = mx + 3 * kMat;
   static constexpr int bars = (misc + 64 + 7) & ~7;        // 7 x uint64
   static constexpr int total = bars + 7 * 8;
   static_assert(total <= kTcMaxSmem, "two CTAs per SM");
+  static_assert(TP == kChainC, "tf holds a dense C x C matrix");
   static_assert(sqk % 128 == 0 && sv % 128 == 0 && CS::bytes % 128 == 0, "TMA destinations");
 };
 
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   using CL = ChainLayout;
   using CS = ChainStage;
   constexpr int C = kChainC, NMAX = kChainC, NC = Ly::NC, R1 = Ly::R1, KP = Ly::KP, KH = KP / 2;
-  constexpr int TP = CL::TP, NH = C / 2, LB = 8;
+  constexpr int NH = C / 2, LB = 8;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *st = smem + CL::stage;
@@ -120,6 +126,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   float *cac = reinterpret_cast<float *>(smem + CL::cac);
   float *Lm = reinterpret_cast<float *>(smem + CL::lm);
   float *Qm = reinterpret_cast<float *>(smem + CL::qm);
+  float *Mx = reinterpret_cast<float *>(smem + CL::mx);  // three C x C matrices
   int *misc = reinterpret_cast<int *>(smem + CL::misc);
   // misc[0] error flag, [2] last arriver, [3] TMEM base
   float *fmisc = reinterpret_cast<float *>(misc + 8);  // [0] gamma_end, [1] gamma_acc
@@ -358,23 +365,22 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       }
       wait_on(mma_bar, mma_waits);
       ptx::tc_fence_after();
-      if (warp == 0) {
-        // lane j < C: k_j.[k_n | q_n] = column n + column n + NC
-        float g0[32], g1[32];
-        ptx::tmem_ld32(tq + Ly::cD1, g0);
-        ptx::tmem_ld32(tq + Ly::cD1 + 32, g1);
+      if (warp == 0 || warp == 4) {
+        // lane j < C: k_j.k_n = column n + column NC + n (warp 0), k_j.q_n =
+        // column NMAX + n + column NC + NMAX + n (warp 4)
+        const int c0 = warp == 0 ? 0 : NMAX;
+        float g0[16], g1[16];
+        ptx::tmem_ld16(tq + Ly::cD1 + c0, g0);
+        ptx::tmem_ld16(tq + Ly::cD1 + NC + c0, g1);
         ptx::tmem_wait_ld();
-        const int jr = tid;
+        const int jr = tid & 31;
+        float *dst = warp == 0 ? gkk : gkq;
         if (jr < C) {
 #pragma unroll
           for (int n = 0; n < C; ++n) {
-            const float kk = g0[n] + g1[n], kq = g0[NMAX + n] + g1[NMAX + n];
-            if (n > jr) {
-              const int e = n * (n - 1) / 2 + (n - 1 - jr);
-              gkk[e] = kk;
-              gkq[e] = kq;
-            }
-            if (n == jr) kqn[n] = kq;
+            const float v = g0[n] + g1[n];
+            if (n > jr) dst[n * (n - 1) / 2 + (n - 1 - jr)] = v;
+            if (warp == 4 && n == jr) kqn[n] = v;
           }
         }
       }
@@ -384,44 +390,85 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       // ---- T = (I + L)^-1 with L = diag(b a) M, and W = Q T, for the
       // chunk's chain: L[n][j] = b_n a_n g(j->n-1) k_j.k_n, Q[n][j] =
       // a_n g(j->n-1) k_j.q_n (j < n), Q[n][n] = k_n.q_n ----
+      // C x C products of lower-triangular matrices, one entry (n, m) per
+      // thread: row n of X (row-major) times column m of Y (row m of Y^T),
+      // four 16-byte loads each; rows MP floats apart (Tf: C)
+      const int en = tid >> 4, em = tid & 15;
+      constexpr int MP = CL::kMP;
+      auto row_dot = [&](const float *X, int xp, const float *YT) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(X + en * xp);
+        const float4 *y4 = reinterpret_cast<const float4 *>(YT + em * MP);
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < C / 4; ++q) {
+          const float4 xa = x4[q], ya = y4[q];
+          acc = fmaf(xa.x, ya.x, fmaf(xa.y, ya.y, fmaf(xa.z, ya.z, fmaf(xa.w, ya.w, acc))));
+        }
+        return acc;
+      };
+      // matrices: Lm, LmT, Ma, MaT and Tf, reused as the steps go
+      float *LmT = Mx, *Ma = Mx + C * MP, *MaT = Mx + 2 * C * MP;
       {
-        const int n = tid >> 4, j = tid & 15;  // entry (n, j), C * C = 256 threads
+        // entry (n, j): g(j -> n-1) = a_(j+1) ... a_(n-1), a suffix product over
+        // the half-warp of row n (lane u holds a_u for u < n, else 1)
+        const int n = en, j = em;
+        float sfx = j < n ? an[j] : 1.f;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+          const float t = __shfl_down_sync(0xffffffffu, sfx, o, 16);
+          if (j + o < 16) sfx *= t;
+        }
+        const float g_next = __shfl_down_sync(0xffffffffu, sfx, 1, 16);
+        const float g = j < 15 ? g_next : 1.f;
         float lv = 0.f, qv = j == n ? kqn[n] : 0.f;
         if (j < n) {
-          float g = 1.f;
-          for (int u = j + 1; u < n; ++u) g *= an[u];
           const int e = n * (n - 1) / 2 + (n - 1 - j);
           lv = bn[n] * an[n] * g * gkk[e];
           qv = an[n] * g * gkq[e];
         }
-        Lm[n * C + j] = lv;
-        Qm[n * C + j] = qv;
+        Lm[n * MP + j] = lv;
+        LmT[j * MP + n] = lv;
+        Qm[n * MP + j] = qv;
+      }
+      __syncthreads();
+      // T = (I + L)^-1 = (I - L)(I + L^2)(I + L^4)(I + L^8), since L^16 = 0
+      {
+        const float l2 = row_dot(Lm, MP, LmT);  // L^2 -> Ma, MaT
+        Ma[en * MP + em] = l2;
+        MaT[em * MP + en] = l2;
       }
       __syncthreads();
       {
-        // column m of T on half-warp m: row n of (I + L) T = I gives
-        // T[n][m] = [n == m] - sum_{j<n} L[n][j] T[j][m]; lane j keeps T[j][m]
-        const int m = tid >> 4, jj = tid & 15;
-        float tcol = jj == m ? 1.f : 0.f;
-#pragma unroll
-        for (int n = 1; n < C; ++n) {
-          float t = jj < n ? Lm[n * C + jj] * tcol : 0.f;
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-          const float val = (n == m ? 1.f : 0.f) - t;
-          if (jj == n) tcol = val;
-        }
-        Tf[jj * TP + m] = tcol;
+        const float l4 = row_dot(Ma, MP, MaT);  // L^4 -> Lm, LmT
+        const float la = row_dot(Lm, MP, MaT);  // L L^2
+        const float id = en == em ? 1.f : 0.f;
+        const float p = id - Lm[en * MP + em] + Ma[en * MP + em] - la;  // P = (I - L)(I + L^2)
+        __syncthreads();  // every read of L and L^2 done
+        Tf[en * C + em] = p;
+        Lm[en * MP + em] = l4;
+        LmT[em * MP + en] = l4;
       }
       __syncthreads();
       {
-        // W[n][m] = sum_j Q[n][j] T[j][m]; T and W entries (n >= m) -> [T|W]
-        const int n = tid >> 4, m = tid & 15;
+        const float l8 = row_dot(Lm, MP, LmT);              // L^8
+        const float p2 = Tf[en * C + em] + row_dot(Tf, C, LmT);  // P (I + L^4)
+        __syncthreads();  // every read of P and L^4 done
+        Ma[en * MP + em] = p2;
+        MaT[em * MP + en] = l8;
+      }
+      __syncthreads();
+      {
+        const float t = Ma[en * MP + em] + row_dot(Ma, MP, MaT);  // P (I + L^4)(I + L^8)
+        Tf[en * C + em] = t;                                  // T
+        LmT[em * MP + en] = t;                                 // T^T
+      }
+      __syncthreads();
+      {
+        // W[n][m] = Q[n] . T[:, m]; T and W entries (n >= m) -> [T|W]
+        const int n = en, m = em;
         if (m <= n) {
-          float wv = 0.f;
-#pragma unroll
-          for (int j = 0; j < C; ++j) wv = fmaf(Qm[n * C + j], Tf[j * TP + m], wv);
-          const float tv = Tf[n * TP + m];
+          const float wv = row_dot(Qm, MP, LmT);
+          const float tv = Tf[n * C + m];
           uint16_t th, tl, wh, wl;
           split_bf16(tv, th, tl);
           split_bf16(wv, wh, wl);
