@@ -55,7 +55,7 @@ def lib():
             _lib = ctypes.CDLL(build())
             for name in ("lbxo_check_tree", "lbxo_conv_lb", "lbxo_tree_conv",
                          "lbxo_deltanet_head", "lbxo_persist_conv_lb", "lbxo_verify_heads",
-                         "lbxo_tree_deltanet", "lbxo_tree_persist"):
+                         "lbxo_tree_deltanet", "lbxo_tree_persist", "lbxo_accept_walk"):
                 getattr(_lib, name).restype = ctypes.c_int
         return _lib
 
@@ -199,3 +199,20 @@ def verify_step_full(w, inp: dict, form: int = FORM_PATH, n_threads: int = 0):
             cache[l, s] = persist_conv_lb(w.N, w.C, w.K, inp["x"][l, b], inp["conv_cache"][l, s],
                                           inp["parent"][b], inp["accepted"][b])
     return o, state, cache
+
+
+def accept_walk(logits: np.ndarray, draft: np.ndarray, parent: np.ndarray):
+    """Verify argmax and greedy acceptance walk (see lbx_oracle.c).
+
+    logits float32 [Bq][N][V], draft and parent int32 [Bq][N].  Returns
+    (argmax int32 [Bq][N], accepted int32 [Bq], next int32 [Bq])."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    Bq, N, V = lg.shape
+    dr = np.ascontiguousarray(draft, dtype=np.int32).reshape(Bq, N)
+    pa = np.ascontiguousarray(parent, dtype=np.int32).reshape(Bq, N)
+    am = np.zeros((Bq, N), dtype=np.int32)
+    acc = np.zeros(Bq, dtype=np.int32)
+    nxt = np.zeros(Bq, dtype=np.int32)
+    _check(lib().lbxo_accept_walk(ctypes.c_int(Bq), ctypes.c_int(N), ctypes.c_int(V), _p(lg),
+                                  _p(dr), _p(pa), _p(am), _p(acc), _p(nxt)), "lbxo_accept_walk")
+    return am, acc, nxt

@@ -529,3 +529,66 @@ int lbxo_tree_persist(const lbxo_cfg *cfg, const uint16_t *x, const float *node_
   free(tmp);
   return LBXO_OK;
 }
+
+/* ---- verify argmax and greedy acceptance walk -------------------------------
+ *
+ * Sources: Lucebox hub README, section "GPU draft top-K & verify-argmax
+ * (DFlash)" (the target's per-node argmax over the vocabulary, taken on the
+ * device from the logits buffer, decides acceptance), and the same README's
+ * serving notes (temperature 0, greedy decoding, gives the highest acceptance).
+ * The pages print no rule; the plain greedy reading is taken:
+ *   - the target's choice at node n is the argmax of its logits row n: the
+ *     largest value; NaN ranks below every number; among equal values (and
+ *     in an all-NaN row) the lowest index;
+ *   - the walk starts at the root (node 0, the last accepted token, always
+ *     kept); at node u it moves to the lowest-index child c of u whose draft
+ *     token equals the target's choice at u, and stops when there is none;
+ *   - accepted[b] = the node where it stops; next[b] = the target's choice at
+ *     that node (the token that follows the accepted path).
+ * logits [Bq][N][V] fp32, draft [Bq][N] int32 (draft[b][0] is not read),
+ * parent [Bq][N] int32; argmax [Bq][N], accepted [Bq], next [Bq] int32 out.
+ */
+
+/* 1 if value a at index ia ranks above value b at index ib. */
+static int ranks_above(float a, int ia, float b, int ib) {
+  int na = isnan(a), nb = isnan(b);
+  if (na && nb) return ia < ib;
+  if (na) return 0;
+  if (nb) return 1;
+  if (a > b) return 1;
+  if (a < b) return 0;
+  return ia < ib;
+}
+
+int lbxo_accept_walk(int Bq, int N, int V, const float *logits, const int32_t *draft,
+                     const int32_t *parent, int32_t *argmax_out, int32_t *accepted_out,
+                     int32_t *next_out) {
+  if (Bq < 1 || N < 1 || V < 1) return LBXO_EINVAL;
+  for (int bb = 0; bb < Bq; ++bb)
+    if (lbxo_check_tree(parent + (size_t)bb * N, N) != LBXO_OK) return LBXO_ETREE;
+  for (int bb = 0; bb < Bq; ++bb) {
+    int32_t *am = argmax_out + (size_t)bb * N;
+    for (int n = 0; n < N; ++n) {
+      const float *row = logits + ((size_t)bb * N + n) * V;
+      int best = 0;
+      for (int v = 1; v < V; ++v)
+        if (ranks_above(row[v], v, row[best], best)) best = v;
+      am[n] = best;
+    }
+    const int32_t *par = parent + (size_t)bb * N, *dr = draft + (size_t)bb * N;
+    int u = 0;
+    for (;;) {
+      int next = -1;
+      for (int c = u + 1; c < N; ++c)
+        if (par[c] == u && dr[c] == am[u]) {
+          next = c;
+          break;
+        }
+      if (next < 0) break;
+      u = next;
+    }
+    accepted_out[bb] = u;
+    next_out[bb] = am[u];
+  }
+  return LBXO_OK;
+}
