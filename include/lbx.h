@@ -65,6 +65,7 @@ extern "C" {
 #define LBX_MAX_TREE_NODES 64 /* tree mode: N <= 64 nodes per request          */
 #define LBX_CHAIN_CHUNK 64    /* chunked (chain) mode processes 64 tokens/chunk */
 #define LBX_MAX_CONV_WIDTH 4  /* 1 <= K <= 4                                    */
+#define LBX_ACCEPT_MAX_NODES 4096 /* lbx_accept_walk: N <= 4096 nodes         */
 
 /* Modes of lbx_verify_step. */
 #define LBX_MODE_AUTO 0    /* tree if N <= LBX_MAX_TREE_NODES, else chunked     */
@@ -206,6 +207,45 @@ int lbx_verify_step_noalloc(const lbx_cfg *cfg, const uint16_t *x, const uint16_
                             const uint16_t *a, const uint16_t *b, const int32_t *parent,
                             const int32_t *slot, const int32_t *accepted, float *state,
                             float *conv_cache, float *o, int32_t *d_status, cudaStream_t stream);
+
+/* Bytes of workspace lbx_accept_walk needs (0 on bad sizes).  It must be
+ * zero-filled once before its first use (it holds one arrival counter per
+ * request, which every call that runs to completion leaves at zero, and the
+ * per-slice partial results); two calls that run at the same time must not
+ * share it. */
+size_t lbx_accept_workspace_size(int Bq, int N, int V);
+
+/*
+ * Verify argmax and greedy acceptance walk, on the device (Lucebox hub README,
+ * "GPU draft top-K & verify-argmax (DFlash)": the target's per-node argmax is
+ * taken from the logits buffer in place, so no vocabulary x nodes copy goes to
+ * the host; greedy decoding, per the same README's serving notes, is the
+ * high-acceptance mode).  Its accepted[] output feeds lbx_verify_step /
+ * lbx_tree_persist directly, with no host round trip.
+ *   logits [Bq][N][V] fp32 (4-byte aligned): the target's scores after each
+ *     node (row n = the distribution of the token that follows node n);
+ *   draft [Bq][N] int32: the draft token each node carries (node 0, the
+ *     root = the last accepted token, is not read); parent [Bq][N] int32 as
+ *     for lbx_verify_step (parent[0] = -1, parent[i] in [0, i));
+ *   argmax_out [Bq][N] int32 (may be NULL): the target's choice at each node,
+ *     the index of the largest logit, NaN ranking below every number, the
+ *     lowest index among equal values (and in an all-NaN row);
+ *   accepted_out [Bq] int32: the node where the walk stops -- from the root,
+ *     repeatedly step to the lowest-index child whose draft token equals the
+ *     target's choice at the current node;
+ *   next_out [Bq] int32: the target's choice at the accepted node (the token
+ *     that follows the accepted path).
+ * All pointers are device pointers owned by the caller; the call is
+ * asynchronous on `stream`.  Returns LBX_EINVAL for bad sizes (N >
+ * LBX_ACCEPT_MAX_NODES), NULL or misaligned pointers or a short workspace,
+ * LBX_ECUDA if the launch fails.  A request whose parent array breaks the
+ * tree rules stores LBX_ETREE in *d_status (if not NULL) and writes none of
+ * its outputs.  Draft tokens outside [0, V) never match.
+ */
+int lbx_accept_walk(int Bq, int N, int V, const float *logits, const int32_t *draft,
+                    const int32_t *parent, int32_t *argmax_out, int32_t *accepted_out,
+                    int32_t *next_out, void *workspace, size_t workspace_bytes,
+                    int32_t *d_status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -208,3 +208,44 @@ def make_inputs(w: Workload, seed: Optional[int] = None,
 
     return dict(x=x, conv_w=conv_w, conv_cache=conv_cache, a=a, b=bg,
                 state=state, parent=parent, slot=slots, accepted=accepted)
+
+
+# ---- acceptance walk inputs -------------------------------------------------
+
+# Vocabulary of the synthetic target: a 152K-entry vocabulary, the size class
+# of the 27B target's tokenizer (the pages give no figure).
+ACCEPT_VOCAB = 152064
+
+
+def make_accept_inputs(Bq: int, N: int, V: int, seed: int, tree: str = "ddtree",
+                       p_plant: float = 0.7, ties: bool = False) -> dict:
+    """Seeded inputs of the verify argmax / acceptance walk.
+
+    logits ~ N(0, 1) fp32 [Bq][N][V]; draft tokens uniform on [0, V) with
+    distinct siblings (while V allows); trees as for the verify step.  To make acceptance
+    paths longer than chance, for a fraction p_plant of the nodes one child's
+    draft token is planted as the node's top score (logit 8 + U(0,1), above
+    any N(0, 1) draw at these sizes); with ``ties`` a second child gets the
+    same planted value at another token (the lower token index then wins)."""
+    rng = _rng(seed, 77)
+    logits = rng.standard_normal((Bq, N, V), dtype=np.float32)
+    draft = np.zeros((Bq, N), dtype=np.int32)
+    parent = np.zeros((Bq, N), dtype=np.int32)
+    for b in range(Bq):
+        par = make_tree(rng, N, tree)
+        parent[b] = par
+        for u in range(N):
+            kids = np.flatnonzero(par == u)
+            if len(kids) == 0:
+                continue
+            # distinct siblings while the vocabulary allows it
+            toks = rng.choice(V, size=len(kids), replace=len(kids) > V).astype(np.int32)
+            draft[b, kids] = toks
+            if rng.random() < p_plant:
+                pick = int(rng.integers(0, len(kids)))
+                val = np.float32(8.0 + rng.random())
+                logits[b, u, toks[pick]] = val
+                if ties and len(kids) > 1:
+                    other = int((pick + 1) % len(kids))
+                    logits[b, u, toks[other]] = val
+    return {"logits": logits, "draft": draft, "parent": parent}

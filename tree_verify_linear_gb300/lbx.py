@@ -26,7 +26,9 @@ LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED, LBX_MODE_TREE_CUDA_CORES = 0, 1,
 
 # Every function the header declares, in header order.
 EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
-           "lbx_tree_persist", "lbx_verify_step", "lbx_verify_step_noalloc")
+           "lbx_tree_persist", "lbx_verify_step", "lbx_verify_step_noalloc",
+           "lbx_accept_workspace_size", "lbx_accept_walk")
+LBX_ACCEPT_MAX_NODES = 4096
 LBX_NOALLOC_MAX_GROUPS = 65536
 
 
@@ -68,6 +70,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lbx_verify_step.argtypes = [vp] * 11 + [vp, ctypes.c_size_t, vp, vp]
         lib.lbx_verify_step_noalloc.restype = i32
         lib.lbx_verify_step_noalloc.argtypes = [vp] * 13
+        lib.lbx_accept_workspace_size.restype = ctypes.c_size_t
+        lib.lbx_accept_workspace_size.argtypes = [i32, i32, i32]
+        lib.lbx_accept_walk.restype = i32
+        lib.lbx_accept_walk.argtypes = [i32, i32, i32] + [vp] * 6 + [vp, ctypes.c_size_t, vp, vp]
         _lib = lib
     return _lib
 
@@ -181,3 +187,27 @@ def new_workspace(cfg: lbx_cfg, device="cuda") -> torch.Tensor:
     if n == 0:
         raise LbxError("lbx_workspace_size", LBX_EINVAL)
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def lbx_accept_workspace_size(Bq: int, N: int, V: int) -> int:
+    return int(load().lbx_accept_workspace_size(Bq, N, V))
+
+
+def new_accept_workspace(Bq: int, N: int, V: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of lbx_accept_workspace_size(Bq, N, V) bytes."""
+    n = lbx_accept_workspace_size(Bq, N, V)
+    if n == 0:
+        raise LbxError("lbx_accept_workspace_size", LBX_EINVAL)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def lbx_accept_walk(logits, draft, parent, accepted_out, next_out, workspace, argmax_out=None,
+                    d_status=None, stream=None):
+    """Verify argmax and greedy acceptance walk; logits float32 [Bq][N][V]."""
+    Bq, N, V = logits.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("lbx_accept_walk", load().lbx_accept_walk(
+        Bq, N, V, _f32(logits, "logits"), _i32(draft, "draft"), _i32(parent, "parent"),
+        _i32(argmax_out, "argmax_out"), _i32(accepted_out, "accepted_out"),
+        _i32(next_out, "next_out"), _ptr(workspace, None, "workspace"), ws_bytes,
+        _i32(d_status, "d_status"), _stream(stream)))
