@@ -11,7 +11,9 @@ with the step's inputs copied from pinned host memory and o copied back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lbx|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--op verify|accept]
+`--op accept` times lbx_accept_walk (verify argmax + greedy acceptance walk)
+on a 5-request serving batch instead (a separate JSON line of its own).
 Under torchrun each rank runs an independent replica (the path needs no
 exchange between GPUs); value is the sum over ranks of the work done divided
 by the slowest rank's time.
@@ -383,6 +385,124 @@ def run_lbx(args, w):
     print(json.dumps(line))
 
 
+def run_accept(args):
+    """Times lbx_accept_walk (verify argmax + greedy acceptance walk) on a
+    5-request serving batch of budget-22 trees and a 152K vocabulary.  Three
+    logits buffers are used in turn (3 x 67 MB > L2), so each call reads its
+    logits from HBM."""
+    import torch
+    from tree_verify_linear_gb300 import lbx
+    from tree_verify_linear_gb300.inputs import ACCEPT_VOCAB, make_accept_inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lbx.load()
+    Bq, N, V = 5, 22, ACCEPT_VOCAB
+    sets = [make_accept_inputs(Bq, N, V, seed=3001 + 97 * rank + i) for i in range(3)]
+    lg = [torch.from_numpy(x["logits"]).to(dev) for x in sets]
+    dr = [torch.from_numpy(x["draft"]).to(dev) for x in sets]
+    pa = [torch.from_numpy(x["parent"]).to(dev) for x in sets]
+    acc = torch.zeros(Bq, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(Bq, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = lbx.new_accept_workspace(Bq, N, V, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(i):
+        k = i % 3
+        lbx.lbx_accept_walk(lg[k], dr[k], pa[k], acc, nxt, ws, d_status=status, stream=stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    gpu_id = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid) if uuid else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    us = 1e3 * ms / args.steps
+
+    # end to end: the draft tokens and parents from pinned host memory, the
+    # accepted nodes and next tokens back (the logits are produced on the
+    # device by the target's forward and stay there)
+    hd = [x["draft"] for x in sets]
+    h_dr = torch.from_numpy(hd[0]).pin_memory()
+    h_pa = torch.from_numpy(sets[0]["parent"]).pin_memory()
+    h_acc = torch.zeros(Bq, dtype=torch.int32).pin_memory()
+    h_nxt = torch.zeros(Bq, dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e(i):
+        dr[0].copy_(h_dr, non_blocking=True)
+        pa[0].copy_(h_pa, non_blocking=True)
+        lbx.lbx_accept_walk(lg[i % 3], dr[0], pa[0], acc, nxt, ws, d_status=status, stream=stream)
+        h_acc.copy_(acc, non_blocking=True)
+        h_nxt.copy_(nxt, non_blocking=True)
+
+    for i in range(3):
+        e2e(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = 1e3 * max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    if rank != 0:
+        return
+    import oracle  # CPU baseline leg only
+    cpu = None
+    if not args.no_cpu_baseline:
+        t0, n = time.time(), 0
+        while time.time() - t0 < min(args.cpu_seconds, 10.0):
+            oracle.accept_walk(sets[n % 3]["logits"], sets[n % 3]["draft"], sets[n % 3]["parent"])
+            n += 1
+        cpu = {"value": 1e6 * (time.time() - t0) / n, "unit": "us per call", "cores": 1,
+               "kind": "oracle", "sample": f"{n} whole calls (5 x 22 x {V} logits)"}
+    peak, peak_kind = read_peaks()
+    alg = Bq * N * V * 4 + 2 * Bq * N * 4 + 2 * Bq * 4
+    achieved = alg / (us / 1e6) / 1e9
+    line = {
+        "metric": "us per verify argmax + acceptance walk", "value": us, "unit": "us per call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"acceptance walk: {Bq} requests, budget-{N} DDTree-shaped "
+                               f"trees, vocabulary {V}",
+                   "Bq": Bq, "N": N, "V": V, "parallelism": f"replicas x{world}",
+                   "l2": "three logits buffers in turn (3 x 67 MB > L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes": alg, "kernel": "accept_walk_kernel",
+                     "timed": "whole lbx_accept_walk call"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us per call",
+                "h2d_bytes_per_step": 2 * Bq * N * 4, "d2h_bytes_per_step": 2 * Bq * 4,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,9 +512,20 @@ def main():
     ap.add_argument("--workload", default="step27b", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=("verify", "accept"), default="verify",
+                    help="verify: lbx_verify_step on --workload (the headline); accept: "
+                         "lbx_accept_walk on a serving batch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
+    if args.op == "accept":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "--op accept times the library only; its oracle is the "
+                              "cpu_baseline field"}))
+            return
+        run_accept(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -35,12 +35,29 @@ __device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
+// Best (value, index) so far; index kNone = nothing seen yet.
+constexpr int kNone = 0x7fffffff;
 struct Best {
   float v;
   int i;
 };
 __device__ __forceinline__ void take(Best &x, float v, int i) {
-  if (ranks_above(v, i, x.v, x.i)) x.v = v, x.i = i;
+  if (i != kNone && (x.i == kNone || ranks_above(v, i, x.v, x.i))) x.v = v, x.i = i;
+}
+// Four consecutive values from index i on, visited after every lower index
+// of this thread: without NaN a strict > keeps the lowest index of a tie.
+__device__ __forceinline__ void take4(Best &x, const float4 &f, int i) {
+  if (f.x == f.x && f.y == f.y && f.z == f.z && f.w == f.w) {
+    if (x.i == kNone || !(x.v == x.v) || f.x > x.v) x.v = f.x, x.i = i;  // a number beats NaN
+    if (f.y > x.v) x.v = f.y, x.i = i + 1;
+    if (f.z > x.v) x.v = f.z, x.i = i + 2;
+    if (f.w > x.v) x.v = f.w, x.i = i + 3;
+  } else {
+    take(x, f.x, i);
+    take(x, f.y, i + 1);
+    take(x, f.z, i + 2);
+    take(x, f.w, i + 3);
+  }
 }
 __device__ __forceinline__ Best warp_best(Best x) {
 #pragma unroll
@@ -62,7 +79,7 @@ struct AccArgs {
 };
 
 __global__ void __launch_bounds__(kAccThreads) accept_walk_kernel(const AccArgs A) {
-  extern __shared__ int sh[];  // [N] choices, [N] links
+  extern __shared__ int sh[];  // [N] choices, [N] links, then (S > 1) the slice results
   __shared__ float red_v[kAccThreads / 32];
   __shared__ int red_i[kAccThreads / 32];
   __shared__ int flag;
@@ -74,7 +91,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_walk_kernel(const AccArgs 
   {
     const int lo = (int)(((long long)V * s) / S), hi = (int)(((long long)V * (s + 1)) / S);
     const float *r = A.logits + (size_t)row * V;
-    Best x = {__int_as_float(0x7fffffff), 0x7fffffff};  // NaN at the largest index: ranks last
+    Best x = {0.f, kNone};
     // scalar head up to a 16-byte boundary, float4 body, scalar tail
     const int mis = (int)(((uintptr_t)(r + lo) >> 2) & 3u);
     int a0 = lo + (mis ? 4 - mis : 0);
@@ -82,20 +99,13 @@ __global__ void __launch_bounds__(kAccThreads) accept_walk_kernel(const AccArgs 
     const int nv = (hi - a0) >> 2, a1 = a0 + 4 * nv;
     for (int v = lo + tid; v < a0; v += kAccThreads) take(x, r[v], v);
     const float4 *r4 = reinterpret_cast<const float4 *>(r + a0);
-    for (int q = tid; q < nv; q += kAccThreads) {
-      const float4 f = __ldcs(r4 + q);
-      const int v = a0 + 4 * q;
-      take(x, f.x, v);
-      take(x, f.y, v + 1);
-      take(x, f.z, v + 2);
-      take(x, f.w, v + 3);
-    }
+    for (int q = tid; q < nv; q += kAccThreads) take4(x, __ldcs(r4 + q), a0 + 4 * q);
     for (int v = a1 + tid; v < hi; v += kAccThreads) take(x, r[v], v);
     x = warp_best(x);
     if (lane == 0) red_v[warp] = x.v, red_i[warp] = x.i;
     __syncthreads();
     if (warp == 0) {
-      Best y = {__int_as_float(0x7fffffff), 0x7fffffff};
+      Best y = {0.f, kNone};
       if (lane < kAccThreads / 32) y.v = red_v[lane], y.i = red_i[lane];
       y = warp_best(y);
       if (lane == 0) {
@@ -113,16 +123,29 @@ __global__ void __launch_bounds__(kAccThreads) accept_walk_kernel(const AccArgs 
   int *choice = sh, *link = sh + N;
   const int32_t *par = A.parent + (size_t)b * N, *dr = A.draft + (size_t)b * N;
   int bad = 0;
+  const uint2 *pp = A.part + (size_t)b * N * S;
+  if (S == 1) {
+    for (int n = tid; n < N; n += kAccThreads) choice[n] = (int)__ldcg(pp + n).y;
+  } else {
+    // the slices' results, one load per thread, staged after the two arrays
+    int *stage = sh + 2 * N;
+    for (int k = tid; k < N * S; k += kAccThreads) {
+      const uint2 u = __ldcg(pp + k);
+      stage[2 * k] = (int)u.x;
+      stage[2 * k + 1] = (int)u.y;
+    }
+    __syncthreads();
+    for (int n = tid; n < N; n += kAccThreads) {
+      Best y = {0.f, kNone};
+      for (int k = 0; k < S; ++k)
+        take(y, __int_as_float(stage[2 * (n * S + k)]), stage[2 * (n * S + k) + 1]);
+      choice[n] = y.i;
+    }
+  }
+  __syncthreads();
   for (int n = tid; n < N; n += kAccThreads) {
     const int p = par[n];
     if (n == 0 ? p != -1 : !(p >= 0 && p < n)) bad = 1;
-    Best y = {__int_as_float(0x7fffffff), 0x7fffffff};
-    const uint2 *pp = A.part + ((size_t)b * N + n) * S;
-    for (int k = 0; k < S; ++k) {
-      const uint2 u = __ldcg(pp + k);
-      take(y, __uint_as_float(u.x), (int)u.y);
-    }
-    choice[n] = y.i;
     link[n] = 0x7fffffff;
   }
   bad = __syncthreads_or(bad);
@@ -218,7 +241,8 @@ extern "C" int lbx_accept_walk(int Bq, int N, int V, const float *logits, const 
                                              ((part + 255) & ~(size_t)255));
   const long long grid = (long long)Bq * N * A.S;
   if (grid > 0x7fffffffLL) return LBX_EINVAL;
-  const size_t smem = (size_t)2 * N * sizeof(int);
+  const size_t smem = ((size_t)2 * N + (A.S > 1 ? (size_t)2 * N * A.S : 0)) * sizeof(int);
+  if (smem > 48 * 1024) return LBX_EINVAL;  // not reached: S > 1 only while Bq N < 1024
   lbx::accept_walk_kernel<<<(unsigned)grid, lbx::kAccThreads, smem, stream>>>(A);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
