@@ -55,7 +55,8 @@ def lib():
             _lib = ctypes.CDLL(build())
             for name in ("lbxo_check_tree", "lbxo_conv_lb", "lbxo_tree_conv",
                          "lbxo_deltanet_head", "lbxo_persist_conv_lb", "lbxo_verify_heads",
-                         "lbxo_tree_deltanet", "lbxo_tree_persist", "lbxo_accept_walk"):
+                         "lbxo_tree_deltanet", "lbxo_tree_persist", "lbxo_accept_walk",
+                         "lbxo_ddtree_build"):
                 getattr(_lib, name).restype = ctypes.c_int
         return _lib
 
@@ -216,3 +217,24 @@ def accept_walk(logits: np.ndarray, draft: np.ndarray, parent: np.ndarray):
     _check(lib().lbxo_accept_walk(ctypes.c_int(Bq), ctypes.c_int(N), ctypes.c_int(V), _p(lg),
                                   _p(dr), _p(pa), _p(am), _p(acc), _p(nxt)), "lbxo_accept_walk")
     return am, acc, nxt
+
+
+def ddtree_build(logp: np.ndarray, tok: np.ndarray, root_tok: np.ndarray, B: int):
+    """DDTree construction from draft top-K scores (see lbx_oracle.c).
+
+    logp float32 [Bq][D][K], tok int32 [Bq][D][K], root_tok int32 [Bq].
+    Returns (parent, token, depth int32 [Bq][B], score float32 [Bq][B],
+    n_nodes int32 [Bq])."""
+    lp = np.ascontiguousarray(logp, dtype=np.float32)
+    Bq, D, K = lp.shape
+    tk = np.ascontiguousarray(tok, dtype=np.int32).reshape(Bq, D, K)
+    rt = np.ascontiguousarray(root_tok, dtype=np.int32).reshape(Bq)
+    par = np.zeros((Bq, B), np.int32)
+    tn = np.zeros((Bq, B), np.int32)
+    dp = np.zeros((Bq, B), np.int32)
+    sc = np.zeros((Bq, B), np.float32)
+    nn = np.zeros(Bq, np.int32)
+    _check(lib().lbxo_ddtree_build(ctypes.c_int(Bq), ctypes.c_int(D), ctypes.c_int(K),
+                                   ctypes.c_int(B), _p(lp), _p(tk), _p(rt), _p(par), _p(tn),
+                                   _p(dp), _p(sc), _p(nn)), "lbxo_ddtree_build")
+    return par, tn, dp, sc, nn

@@ -592,3 +592,69 @@ int lbxo_accept_walk(int Bq, int N, int V, const float *logits, const int32_t *d
   }
   return LBXO_OK;
 }
+
+/* ---- DDTree construction from draft top-K scores ----------------------------
+ *
+ * Sources: Lucebox hub README, "Algorithms used" (DDTree: a tree-structured
+ * verify that beats chain verify at the same budget), "Implemented here"
+ * (budget 22 on the RTX 3090) and "GPU draft top-K & verify-argmax (DFlash)"
+ * (the draft's top-K tokens, K in 1..8, and their log-sum-exp, per position).
+ * The pages print no construction rule; the plain reading taken:
+ *   - the draft gives, for each of the D positions after the root, its top-K
+ *     tokens tok[d][k] with log-probabilities logp[d][k];
+ *   - a node at depth d >= 1 is a choice of one of those K tokens at every
+ *     position 0..d-1 along its path; its score is the sum of the path's
+ *     log-probabilities, summed in fp32 from the root down (score(child) =
+ *     score(parent) + logp[depth(parent)][k]);
+ *   - the tree of budget B is built best first: starting from the root
+ *     (score 0), repeatedly add the not-yet-added child of an added node with
+ *     the highest score (ties: the lower parent index, then the lower k),
+ *     until B nodes or no candidate is left; nodes are numbered in the order
+ *     they are added, so parent[i] < i.  This keeps the B highest-scoring
+ *     nodes, the tree that maximises the summed path probability when the
+ *     draft's positions are taken as independent.
+ * logp [Bq][D][K] fp32, tok [Bq][D][K] int32, root_tok [Bq] int32;
+ * out: parent [Bq][B], token [Bq][B], depth [Bq][B] int32, score [Bq][B]
+ * fp32, n_nodes [Bq] int32; unused node slots get parent -1, token -1,
+ * depth -1, score 0.
+ */
+int lbxo_ddtree_build(int Bq, int D, int K, int B, const float *logp, const int32_t *tok,
+                      const int32_t *root_tok, int32_t *parent, int32_t *token, int32_t *depth,
+                      float *score, int32_t *n_nodes) {
+  if (Bq < 1 || D < 0 || K < 1 || B < 1) return LBXO_EINVAL;
+  int *slot = malloc((size_t)B * sizeof *slot); /* the k each node was chosen with */
+  if (!slot) return LBXO_ENOMEM;
+  for (int bb = 0; bb < Bq; ++bb) {
+    const float *lp = logp + (size_t)bb * D * K;
+    const int32_t *tk = tok + (size_t)bb * D * K;
+    int32_t *par = parent + (size_t)bb * B, *tn = token + (size_t)bb * B,
+            *dp = depth + (size_t)bb * B;
+    float *sc = score + (size_t)bb * B;
+    for (int i = 0; i < B; ++i) par[i] = -1, tn[i] = -1, dp[i] = -1, sc[i] = 0.0f, slot[i] = -1;
+    tn[0] = root_tok[bb], dp[0] = 0;
+    int n = 1;
+    while (n < B) {
+      /* every child (u, k) of an added node u that is not added yet */
+      int bu = -1, bk = -1;
+      float bs = 0.0f;
+      for (int u = 0; u < n; ++u) {
+        if (dp[u] >= D) continue;
+        for (int k = 0; k < K; ++k) {
+          int added = 0;
+          for (int c = 1; c < n; ++c)
+            if (par[c] == u && slot[c] == k) added = 1;
+          if (added) continue;
+          const float s = sc[u] + lp[dp[u] * K + k]; /* fp32, root down */
+          /* scan order is (u, k) ascending: a strict > keeps the first of a tie */
+          if (bu < 0 || s > bs) bu = u, bk = k, bs = s;
+        }
+      }
+      if (bu < 0) break;
+      par[n] = bu, slot[n] = bk, tn[n] = tk[dp[bu] * K + bk], dp[n] = dp[bu] + 1, sc[n] = bs;
+      ++n;
+    }
+    n_nodes[bb] = n;
+  }
+  free(slot);
+  return LBXO_OK;
+}
