@@ -66,6 +66,8 @@ extern "C" {
 #define LBX_CHAIN_CHUNK 64    /* chunked (chain) mode processes 64 tokens/chunk */
 #define LBX_MAX_CONV_WIDTH 4  /* 1 <= K <= 4                                    */
 #define LBX_ACCEPT_MAX_NODES 4096 /* lbx_accept_walk: N <= 4096 nodes         */
+#define LBX_DDTREE_MAX_K 8        /* lbx_ddtree_build: top-K, 1 <= K <= 8       */
+#define LBX_DDTREE_MAX_DEPTH 64   /* lbx_ddtree_build: draft positions D <= 64  */
 
 /* Modes of lbx_verify_step. */
 #define LBX_MODE_AUTO 0    /* tree if N <= LBX_MAX_TREE_NODES, else chunked     */
@@ -246,6 +248,37 @@ int lbx_accept_walk(int Bq, int N, int V, const float *logits, const int32_t *dr
                     const int32_t *parent, int32_t *argmax_out, int32_t *accepted_out,
                     int32_t *next_out, void *workspace, size_t workspace_bytes,
                     int32_t *d_status, cudaStream_t stream);
+
+/*
+ * DDTree construction from the draft's top-K scores, on the device (Lucebox
+ * hub README: DDTree, the tree-structured verify that beats chain verify at
+ * the same budget, in "Algorithms used"; budget 22 on the RTX 3090 in
+ * "Implemented here"; the draft's per-position top-K tokens, K in 1..8, in
+ * "GPU draft top-K & verify-argmax (DFlash)").  The output parent array is
+ * topologically numbered and feeds lbx_verify_step as is.
+ *   logp [Bq][D][K] fp32: log-probabilities of the draft's top-K tokens at
+ *     each of the D positions after the root (any order within a position;
+ *     -inf allowed, NaN not);
+ *   tok [Bq][D][K] int32: those tokens; root_tok [Bq] int32: the root's
+ *     token (the last accepted token);
+ *   parent_out, token_out [Bq][B] int32; depth_out [Bq][B] int32 and
+ *     score_out [Bq][B] fp32 may be NULL; n_nodes_out [Bq] int32.
+ * A node's score is the sum of the log-probabilities on its path, added in
+ * fp32 from the root down; the tree is built best first: from the root
+ * (score 0) the not-yet-added child of an added node with the highest score
+ * joins next -- ties: the lower parent index, then the lower k -- until B
+ * nodes or no candidate is left (n_nodes < B only when the whole trie of
+ * depth D has fewer nodes).  Nodes are numbered in joining order; unused
+ * slots get parent, token and depth -1 and score 0.  Device pointers owned
+ * by the caller; asynchronous on `stream`.  Returns LBX_EINVAL for sizes
+ * outside 1 <= B <= LBX_MAX_TREE_NODES, 1 <= K <= LBX_DDTREE_MAX_K,
+ * 0 <= D <= LBX_DDTREE_MAX_DEPTH or NULL / misaligned pointers, LBX_ECUDA
+ * if the launch fails.
+ */
+int lbx_ddtree_build(int Bq, int D, int K, int B, const float *logp, const int32_t *tok,
+                     const int32_t *root_tok, int32_t *parent_out, int32_t *token_out,
+                     int32_t *depth_out, float *score_out, int32_t *n_nodes_out,
+                     cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -249,3 +249,20 @@ def make_accept_inputs(Bq: int, N: int, V: int, seed: int, tree: str = "ddtree",
                     other = int((pick + 1) % len(kids))
                     logits[b, u, toks[other]] = val
     return {"logits": logits, "draft": draft, "parent": parent}
+
+
+def make_draft_topk(Bq: int, D: int, K: int, V: int, seed: int) -> dict:
+    """Seeded draft top-K scores for the DDTree construction: per request and
+    position, K distinct tokens uniform on [0, V) and the log of K
+    probabilities drawn as the top K of a Dirichlet(1) over K + 8 outcomes,
+    sorted descending; root tokens uniform on [0, V)."""
+    rng = _rng(seed, 88)
+    p = rng.dirichlet(np.ones(K + 8), size=(Bq, D))
+    p = -np.sort(-p, axis=-1)[..., :K]
+    logp = np.log(p).astype(np.float32)
+    tok = np.empty((Bq, D, K), dtype=np.int32)
+    for b in range(Bq):
+        for d in range(D):
+            tok[b, d] = rng.choice(V, size=K, replace=False)
+    root = rng.integers(0, V, size=Bq).astype(np.int32)
+    return {"logp": logp, "tok": tok, "root_tok": root}

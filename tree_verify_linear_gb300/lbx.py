@@ -27,8 +27,9 @@ LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED, LBX_MODE_TREE_CUDA_CORES = 0, 1,
 # Every function the header declares, in header order.
 EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
            "lbx_tree_persist", "lbx_verify_step", "lbx_verify_step_noalloc",
-           "lbx_accept_workspace_size", "lbx_accept_walk")
+           "lbx_accept_workspace_size", "lbx_accept_walk", "lbx_ddtree_build")
 LBX_ACCEPT_MAX_NODES = 4096
+LBX_DDTREE_MAX_K, LBX_DDTREE_MAX_DEPTH = 8, 64
 LBX_NOALLOC_MAX_GROUPS = 65536
 
 
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lbx_accept_workspace_size.argtypes = [i32, i32, i32]
         lib.lbx_accept_walk.restype = i32
         lib.lbx_accept_walk.argtypes = [i32, i32, i32] + [vp] * 6 + [vp, ctypes.c_size_t, vp, vp]
+        lib.lbx_ddtree_build.restype = i32
+        lib.lbx_ddtree_build.argtypes = [i32, i32, i32, i32] + [vp] * 9
         _lib = lib
     return _lib
 
@@ -211,3 +214,15 @@ def lbx_accept_walk(logits, draft, parent, accepted_out, next_out, workspace, ar
         _i32(argmax_out, "argmax_out"), _i32(accepted_out, "accepted_out"),
         _i32(next_out, "next_out"), _ptr(workspace, None, "workspace"), ws_bytes,
         _i32(d_status, "d_status"), _stream(stream)))
+
+
+def lbx_ddtree_build(logp, tok, root_tok, B, parent_out, token_out, n_nodes_out,
+                     depth_out=None, score_out=None, stream=None):
+    """DDTree construction of budget B from logp float32 [Bq][D][K] and tok
+    int32 [Bq][D][K]."""
+    Bq, D, K = logp.shape
+    _check("lbx_ddtree_build", load().lbx_ddtree_build(
+        Bq, D, K, int(B), _f32(logp, "logp"), _i32(tok, "tok"), _i32(root_tok, "root_tok"),
+        _i32(parent_out, "parent_out"), _i32(token_out, "token_out"),
+        _i32(depth_out, "depth_out"), _f32(score_out, "score_out"),
+        _i32(n_nodes_out, "n_nodes_out"), _stream(stream)))
