@@ -11,9 +11,10 @@ with the step's inputs copied from pinned host memory and o copied back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lbx|reference]
-                       [--workload NAME] [--op verify|accept]
+                       [--workload NAME] [--op verify|accept|ddtree]
 `--op accept` times lbx_accept_walk (verify argmax + greedy acceptance walk)
-on a 5-request serving batch instead (a separate JSON line of its own).
+on a 5-request serving batch instead, `--op ddtree` lbx_ddtree_build (each
+a separate JSON line of its own).
 Under torchrun each rank runs an independent replica (the path needs no
 exchange between GPUs); value is the sum over ranks of the work done divided
 by the slowest rank's time.
@@ -503,6 +504,73 @@ def run_accept(args):
     print(json.dumps(line))
 
 
+def run_ddtree(args):
+    """Times lbx_ddtree_build: budget-22 trees for 5 requests from a
+    16-position draft block with top-8 tokens per position.  The kernel is a
+    chain of 21 dependent selection rounds per request (one warp each): it
+    is bound by latency, not by bytes or arithmetic, so no roofline fraction
+    is given."""
+    import torch
+    from tree_verify_linear_gb300 import lbx
+    from tree_verify_linear_gb300.inputs import ACCEPT_VOCAB, make_draft_topk
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lbx.load()
+    Bq, D, K, B = 5, 16, 8, 22
+    d = make_draft_topk(Bq, D, K, ACCEPT_VOCAB, seed=5001 + rank)
+    lp = torch.from_numpy(d["logp"]).to(dev)
+    tk = torch.from_numpy(d["tok"]).to(dev)
+    rt = torch.from_numpy(d["root_tok"]).to(dev)
+    par = torch.zeros((Bq, B), dtype=torch.int32, device=dev)
+    tn = torch.zeros((Bq, B), dtype=torch.int32, device=dev)
+    nn = torch.zeros(Bq, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        lbx.lbx_ddtree_build(lp, tk, rt, B, par, tn, nn, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    if rank != 0:
+        return
+    import oracle  # CPU baseline leg only
+    cpu = None
+    if not args.no_cpu_baseline:
+        t0, n = time.time(), 0
+        while time.time() - t0 < 2.0:
+            oracle.ddtree_build(d["logp"], d["tok"], d["root_tok"], B)
+            n += 1
+        cpu = {"value": 1e6 * (time.time() - t0) / n, "unit": "us per call", "cores": 1,
+               "kind": "oracle", "sample": f"{n} whole calls"}
+    line = {
+        "metric": "us per DDTree construction", "value": us, "unit": "us per call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"DDTree build: {Bq} requests, budget {B}, draft block {D}, "
+                               f"top-{K}", "Bq": Bq, "D": D, "K": K, "B": B,
+                   "parallelism": f"replicas x{world}", "l2": "inputs of 5 KB (latency-bound)"},
+        "roofline": {"bound": "latency", "achieved": None, "peak": None, "unit": None,
+                     "frac": None, "kernel": "ddtree_build_kernel",
+                     "timed": "whole lbx_ddtree_build call"},
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -512,19 +580,19 @@ def main():
     ap.add_argument("--workload", default="step27b", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("verify", "accept"), default="verify",
+    ap.add_argument("--op", choices=("verify", "accept", "ddtree"), default="verify",
                     help="verify: lbx_verify_step on --workload (the headline); accept: "
-                         "lbx_accept_walk on a serving batch")
+                         "lbx_accept_walk on a serving batch; ddtree: lbx_ddtree_build")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
-    if args.op == "accept":
+    if args.op in ("accept", "ddtree"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
-                              "--op accept times the library only; its oracle is the "
+                              f"--op {args.op} times the library only; its oracle is the "
                               "cpu_baseline field"}))
             return
-        run_accept(args)
+        (run_accept if args.op == "accept" else run_ddtree)(args)
         return
     if args.impl == "reference":
         run_reference(args, w)

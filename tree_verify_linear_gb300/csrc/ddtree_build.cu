@@ -41,12 +41,20 @@ __global__ void __launch_bounds__(32 * kDtWarps) ddtree_build_kernel(const DtArg
   __shared__ int c_u[kDtWarps][kDtMaxCand];    // candidate parent (-1: taken)
   __shared__ int c_k[kDtWarps][kDtMaxCand];    // candidate slot k
   __shared__ int n_d[kDtWarps][LBX_MAX_TREE_NODES];
+  __shared__ float t_lp[kDtWarps][LBX_DDTREE_MAX_DEPTH * LBX_DDTREE_MAX_K];  // the request's
+  __shared__ int t_tk[kDtWarps][LBX_DDTREE_MAX_DEPTH * LBX_DDTREE_MAX_K];    // top-K table
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int b = blockIdx.x * kDtWarps + w;
   if (b >= A.Bq) return;
   const int D = A.D, K = A.K, B = A.B;
-  const float *lp = A.logp + (size_t)b * D * K;
-  const int32_t *tk = A.tok + (size_t)b * D * K;
+  // the request's top-K table, staged once (every round reads it)
+  float *lp = t_lp[w];
+  int *tk = t_tk[w];
+  for (int i = lane; i < D * K; i += 32) {
+    lp[i] = A.logp[(size_t)b * D * K + i];
+    tk[i] = A.tok[(size_t)b * D * K + i];
+  }
+  __syncwarp();
   int32_t *par = A.parent + (size_t)b * B, *tn = A.token + (size_t)b * B;
   int32_t *dep = A.depth ? A.depth + (size_t)b * B : nullptr;
   float *sco = A.score ? A.score + (size_t)b * B : nullptr;
