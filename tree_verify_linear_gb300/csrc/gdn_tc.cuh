@@ -159,7 +159,11 @@ struct TcLayout {
   static constexpr int stg = round_up(b2lo + kB2, 128);  // value-head conv inputs
   static constexpr int tb = stg + CS::bytes;           // tree tables
   static constexpr int hr = tb + TabLayout<NMAX>::bytes;  // value-head record
-  static constexpr int misc = hr + HeadLayout<NMAX>::bytes;  // ints, see kernel
+  // v values of the lead warp's rows for its last kVOff nodes, computed by
+  // warps 1..kVOff (float [kVOff][32])
+  static constexpr int kVOff = NMAX / 4 < 7 ? NMAX / 4 : 7;
+  static constexpr int vx = hr + HeadLayout<NMAX>::bytes;
+  static constexpr int misc = vx + kVOff * 128;  // ints, see kernel
   static constexpr int bars = (misc + 64 + 7) & ~7;   // 6 x uint64
   static constexpr int total = bars + 6 * 8;
   static constexpr int smem_bytes = total;
@@ -706,29 +710,50 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
 
     // ================= v of this row for this half's nodes (staged inputs) =================
+    // The lead warp (warp 0) has just issued MMA1, so it computes only its
+    // first NH - kVOff nodes; warps 1..kVOff each compute one of its other
+    // nodes for its 32 rows and pass the values through shared memory.
     wait_on(stg_bar, stg_waits);
     float vv[NH];
+    constexpr int kVOff = Ly::kVOff, kVOwn = NH - kVOff;
+    float *vx = reinterpret_cast<float *>(smem + Ly::vx);
     {
       const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
       const float *cs = reinterpret_cast<const float *>(sg + CS::c);
-      const uint16_t *ws = reinterpret_cast<const uint16_t *>(sg + CS::w) + r * K;
-      float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
-#pragma unroll
-      for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
-        wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
-#pragma unroll
-      for (int i = 0; i < NH; ++i) {
-        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * (n0 + i));
+      // v of channel (row) rr of node n, window element j weighted by wsl[j]
+      auto vconv = [&](int n, int rr, const float (&wsl)[LBX_MAX_CONV_WIDTH]) {
+        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * n);
         const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
         float y = 0.f;
 #pragma unroll
         for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
           const int w = wj[j];
-          const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
-          const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
-          y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
+          const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + rr]);
+          const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + rr];
+          y = fmaf(wsl[j], w >= 0 ? xn : xc, y);
         }
-        vv[i] = silu_fast(y);
+        return silu_fast(y);
+      };
+      auto weights = [&](int rr, float (&wsl)[LBX_MAX_CONV_WIDTH]) {
+        const uint16_t *ws = reinterpret_cast<const uint16_t *>(sg + CS::w) + rr * K;
+#pragma unroll
+        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
+          wsl[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
+      };
+      float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
+      weights(r, wslot);
+      if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < kVOwn; ++i) vv[i] = vconv(n0 + i, r, wslot);
+      } else {
+#pragma unroll
+        for (int i = 0; i < NH; ++i) vv[i] = vconv(n0 + i, r, wslot);
+        if (warp <= kVOff) {
+          const int lane = tid & 31;
+          float w0[LBX_MAX_CONV_WIDTH];
+          weights(lane, w0);
+          vx[(warp - 1) * 32 + lane] = vconv(kVOwn + warp - 1, lane, w0);
+        }
       }
       // this row's value channel of the conv window (only this tile reads it)
       if (hf == 0) {
@@ -743,6 +768,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     }
     ptx::named_sync(1, kTcThreads);  // staging consumed
     if (lead && it + 1 < count) load_block(nx);
+    if (warp == 0) {
+#pragma unroll
+      for (int i = kVOwn; i < NH; ++i) vv[i] = vx[(i - kVOwn) * 32 + (tid & 31)];
+    }
 
     // ================= rhs -> tensor memory =================
     // Accumulator columns are read in aligned blocks of LB covering this

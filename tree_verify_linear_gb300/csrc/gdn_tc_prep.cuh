@@ -298,6 +298,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       for (int p = 0; p < U; ++p) {
         const int u = p * CT + ct;
         const bool act = u < N * GQ;
+        // warps with no node in this pass skip it (u grows with the lane,
+        // so the warp's first lane decides)
+        if (__shfl_sync(0xffffffffu, u, 0) >= N * GQ) continue;
         const int o = act ? u / GQ : 0;
         // window rows: the node, then its ancestors; past the root the
         // cached rows, newest first (-1 - row); taps j >= K read row 0
