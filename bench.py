@@ -45,11 +45,11 @@ UNIT = "node-head updates/s"
 def step_kernels(w):
     """The kernels one lbx_verify_step call launches for this workload (the
     library's own selection rule, default mode): tree mode (N <= 64) with
-    d = 128 and N <= 24 is a prep kernel per key head followed by the
+    d = 128 is a prep kernel per key head followed by the
     tensor-core step kernel; chunked mode (longer chains) with d = 128 is the
     tensor-core chain kernel; the other configurations run one CUDA-core
     kernel."""
-    if w.d == 128 and w.N <= 24:
+    if w.d == 128 and w.N <= 64:
         return ("gdn_qk_prep_kernel", "gdn_step_tc_kernel")
     if w.d == 128 and w.N > 64:
         return ("gdn_chain_tc_kernel",)

@@ -96,10 +96,11 @@ const char *lbx_strerror(int status);
  * must be zero-filled once before its first use; two calls that run at the
  * same time must not share a workspace.  What it holds depends on the kernel
  * the configuration selects:
- *   - the tensor-core step (tree mode, d = 128, N <= 24): the per-request
- *     tree tables and per-(layer, request, key head) records (q/k operand and
- *     Gram entries, about 27 KB each at N <= 24) that its prep kernel writes
- *     and its step kernel reads, rewritten by every call;
+ *   - the tensor-core step (tree mode, d = 128, N <= 64): the per-request
+ *     tree tables, per-(layer, request, key head) q/k operands (24 KB each
+ *     at N <= 24, 64 KB at N <= 64) and per-(layer, request, value head)
+ *     T/W records (2.8 KB at N <= 24, 17 KB at N <= 64) that its prep kernel
+ *     writes and its step kernel reads, rewritten by every call;
  *   - the CUDA-core kernels: one arrival counter per (layer, request, key
  *     head); every call that runs to completion leaves them zero again. */
 size_t lbx_workspace_size(const lbx_cfg *cfg);

@@ -43,11 +43,11 @@ def run_verify(w, inp, mode=lbx.LBX_MODE_AUTO, steps=1, ws=None):
 
 def uses_tensor_cores(w, mode=lbx.LBX_MODE_AUTO) -> bool:
     """Whether lbx_verify_step runs the tensor-core step (tree mode, d = 128,
-    N <= 24), whose workspace holds the prep kernel's records instead of
+    N <= 64), whose workspace holds the prep kernel's records instead of
     arrival counters."""
     if mode == lbx.LBX_MODE_AUTO:
         mode = lbx.LBX_MODE_TREE if w.N <= lbx.LBX_MAX_TREE_NODES else lbx.LBX_MODE_CHUNKED
-    return mode == lbx.LBX_MODE_TREE and w.d == 128 and w.N <= 24
+    return mode == lbx.LBX_MODE_TREE and w.d == 128 and w.N <= 64
 
 
 def counters_cleared(w, ws: np.ndarray, mode=lbx.LBX_MODE_AUTO) -> bool:

@@ -237,8 +237,9 @@ def test_chunked_mode_rejects_a_non_chain():
 
 
 # -------------------------------------------------------------------------
-# Tensor-core kernel (d = 128, tree mode, N <= 24): shapes at its limits,
-# and agreement with the CUDA-core kernel on the same inputs.
+# Tensor-core kernel (d = 128, tree mode, N <= 64; node capacities 8, 16 and
+# 24 at two CTAs per SM, 32 and 64 at one): shapes at its limits, and
+# agreement with the CUDA-core kernel on the same inputs.
 # -------------------------------------------------------------------------
 def tc(**kw):
     base = dict(name="tc", L=2, Bq=2, N=22, Hk=2, Hv=6, d=128, tree="ddtree", accepted="node",
@@ -263,6 +264,15 @@ TC_EDGE = {
     "q_scale": tc(q_scale=float(1 / np.sqrt(128)), seed=1113),
     "leaf": tc(accepted="leaf", seed=1114),
     "many_tiles": tc(L=7, Bq=3, Hk=4, Hv=12, N=22, seed=1115),
+    "n25": tc(N=25, seed=1116),
+    "n32_uniform": tc(N=32, tree="uniform", seed=1117),
+    "n33": tc(N=33, seed=1118),
+    "n40_leaf": tc(N=40, accepted="leaf", seed=1119),
+    "n64_chain": tc(N=64, tree="chain", accepted="last", seed=1120),
+    "n64_uniform": tc(N=64, tree="uniform", seed=1121),
+    "n64_ddtree_b4": tc(N=64, max_children=4, seed=1122),
+    "n64_three_requests": tc(Bq=3, N=64, max_children=4, seed=1123),
+    "n48_k2_g4": tc(N=48, K=2, Hk=1, Hv=4, tree="uniform", seed=1124),
 }
 
 
@@ -275,6 +285,22 @@ def test_tensor_core_edge_cases(name):
     assert status == 0
     check_verify(w, inp, o, st, cc)
     assert counters_cleared(w, ws, lbx.LBX_MODE_TREE)
+
+
+def test_tensor_core_and_cuda_core_kernels_agree_budget64():
+    """Node capacity 64 (one CTA per SM) against the CUDA-core kernel on the
+    budget-64 serving shapes (4 layers of them)."""
+    w = WORKLOADS["serve27b_b64"].replace(L=4)
+    inp = make_inputs(w)
+    o1, s1, c1, st1, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE)
+    o2, s2, c2, st2, _ = run_verify(w, inp, mode=lbx.LBX_MODE_TREE_CUDA_CORES)
+    assert st1 == st2 == 0
+    assert np.abs(o1 - o2).max() <= 1e-4 * np.abs(o2).max()
+    assert c1.tobytes() == c2.tobytes()
+    # the request slots (the spare slots hold a NaN canary, checked elsewhere)
+    used = inp["slot"]
+    rel = np.linalg.norm((s1 - s2)[:, used].reshape(-1)) / np.linalg.norm(s2[:, used].reshape(-1))
+    assert rel <= 1e-5
 
 
 def test_tensor_core_and_cuda_core_kernels_agree_full_step():

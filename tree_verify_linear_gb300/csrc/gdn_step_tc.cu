@@ -99,7 +99,7 @@ int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return LBX_ECUDA;
-  const int slots = kTcCtasPerSm * nsm;
+  const int slots = TcRes<NMAX>::ctas * nsm;
   const int grid = T.n_tiles < slots ? T.n_tiles : slots;
   // programmatic stream serialization: the step kernel may start while the
   // prep kernel's last CTAs run, and waits for it before reading the workspace
@@ -163,13 +163,15 @@ int launch_chain_tc(const StepArgs &A, cudaStream_t st) {
 }
 
 bool step_tc_supported(int d, int N, int chain) {
-  return d == kTcD && !chain && N >= 1 && N <= 24;
+  return d == kTcD && !chain && N >= 1 && N <= 64;
 }
 
 size_t step_tc_workspace_bytes(int L, int Bq, int Hk, int Hv, int N) {
   if (N <= 8) return tc_workspace_bytes<8>(L, Bq, Hk, Hv);
   if (N <= 16) return tc_workspace_bytes<16>(L, Bq, Hk, Hv);
   if (N <= 24) return tc_workspace_bytes<24>(L, Bq, Hk, Hv);
+  if (N <= 32) return tc_workspace_bytes<32>(L, Bq, Hk, Hv);
+  if (N <= 64) return tc_workspace_bytes<64>(L, Bq, Hk, Hv);
   return 0;
 }
 
@@ -179,6 +181,8 @@ int launch_step_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st
   if (A.N <= 8) return launch_tc<8>(A, ws, ws_bytes, st);
   if (A.N <= 16) return launch_tc<16>(A, ws, ws_bytes, st);
   if (A.N <= 24) return launch_tc<24>(A, ws, ws_bytes, st);
+  if (A.N <= 32) return launch_tc<32>(A, ws, ws_bytes, st);
+  if (A.N <= 64) return launch_tc<64>(A, ws, ws_bytes, st);
   return LBX_EINVAL;
 }
 

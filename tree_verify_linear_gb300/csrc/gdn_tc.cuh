@@ -62,6 +62,20 @@ constexpr int kTcMaxSmem = 113 * 1024;             // two CTAs per SM
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Resources of the tree step by node capacity: up to 24 nodes two CTAs share
+// an SM (256 TMEM columns and at most 113 KB of shared memory each); larger
+// capacities (up to 64) take one CTA per SM with all 512 TMEM columns.  The
+// prep kernel handles kPrepHeads value heads at a time (its per-head scratch
+// grows with NMAX^2).
+template <int NMAX>
+struct TcRes {
+  static constexpr int ctas = NMAX <= 24 ? 2 : 1;
+  static constexpr uint32_t tmem_cols = NMAX <= 24 ? 256u : 512u;
+  static constexpr int max_smem = NMAX <= 24 ? 113 * 1024 : 227 * 1024;
+  static constexpr int prep_ctas = NMAX <= 24 ? 4 : 1;
+  static constexpr int prep_heads = NMAX <= 24 ? 4 : 2;
+};
+
 // Staged conv inputs of one 128-channel block for N nodes: raw inputs
 // x[n][128] bf16, cached rows [K-1][128] fp32 (oldest first), weights
 // [128][K] bf16.
@@ -148,7 +162,7 @@ struct TcLayout {
   // the first half of the MMA1 accumulator, the MMA3 accumulator the S0
   // columns.
   static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + R1, cD2 = cD1;
-  static_assert(cA2 + KP <= kTcTmemCols, "tensor memory");
+  static_assert(cA2 + KP <= TcRes<NMAX>::tmem_cols, "tensor memory");
   // byte distance from a T entry of [T|W] to the W entry of the same lane
   static constexpr int kWOff = (NMAX / 8) * KP * 16;
   static_assert(NMAX % 8 == 0, "W rows start at an 8-row group");
@@ -168,16 +182,16 @@ struct TcLayout {
   static constexpr int total = bars + 6 * 8;
   static constexpr int smem_bytes = total;
   static_assert(kB % 1024 == 0, "operand [K|Q] must keep 1024-byte alignment");
-  static_assert(smem_bytes <= kTcMaxSmem, "two CTAs per SM");
+  static_assert(smem_bytes <= TcRes<NMAX>::max_smem, "CTAs per SM");
   static_assert(stg % 128 == 0 && tb % 16 == 0 && hr % 16 == 0 && b2hi % 16 == 0, "alignment");
 };
 
 // Shared memory of the prep kernel (one CTA per key head).  After the conv
 // the staged inputs are dead and the same bytes hold the per-head T scratch
 // and gate vectors of up to kPrepHeads value heads at a time.
-constexpr int kPrepHeads = 4;
 template <int NMAX>
 struct PrepLayout {
+  static constexpr int kPrepHeads = TcRes<NMAX>::prep_heads;
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
   static constexpr int NP = round_up(NMAX, 4);
@@ -432,7 +446,7 @@ __device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t a, uint32_t b1)
 }
 
 template <int NMAX>
-__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
+__global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
     gdn_step_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
@@ -505,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(reinterpret_cast<uint32_t *>(&misc[3]), kTcTmemCols);
+    ptx::tmem_alloc(reinterpret_cast<uint32_t *>(&misc[3]), TcRes<NMAX>::tmem_cols);
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
   }
@@ -783,23 +797,34 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       constexpr int HF = decltype(hfc)::value;
       constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
       constexpr int NL = round_up(SH + NH, LB);
-      float k_hi[NL], k_lo[NL], q_hi[NL], q_lo[NL];
-#pragma unroll
-      for (int b = 0; b < NL / LB; ++b) {
-        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + B0 + b * LB, k_hi + b * LB);
-        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + B0 + b * LB, k_lo + b * LB);
-        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NMAX + B0 + b * LB, q_hi + b * LB);
-        ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + NMAX + B0 + b * LB, q_lo + b * LB);
-      }
-      ptx::tmem_wait_ld();
       // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
       float rhs[NH];
+      // accumulator columns in pieces of CH * LB (all at once for small
+      // halves; 8 columns at a time for the large ones, to bound registers)
+      constexpr int CH = NH > 12 ? 1 : NL / LB;
+      static_assert(CH == NL / LB || SH == 0, "chunked halves start aligned");
 #pragma unroll
-      for (int i = 0; i < NH; ++i) {
-        const int n = N0 + i;
-        const float ag = an[n] * gam[n];
-        rhs[i] = bn[n] * fmaf(-ag, k_hi[SH + i] + k_lo[SH + i], vv[i]);
-        oq[i] = ag * (q_hi[SH + i] + q_lo[SH + i]);
+      for (int c0 = 0; c0 < NL / LB; c0 += CH) {
+        float k_hi[CH * LB], k_lo[CH * LB], q_hi[CH * LB], q_lo[CH * LB];
+#pragma unroll
+        for (int b = 0; b < CH; ++b) {
+          const int cb = B0 + (c0 + b) * LB;
+          ptx::tmem_ld_w<LB>(tq + Ly::cD1 + cb, k_hi + b * LB);
+          ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + cb, k_lo + b * LB);
+          ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NMAX + cb, q_hi + b * LB);
+          ptx::tmem_ld_w<LB>(tq + Ly::cD1 + NC + NMAX + cb, q_lo + b * LB);
+        }
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < CH * LB; ++e) {
+          const int i = c0 * LB + e - SH;  // node N0 + i
+          if (i >= 0 && i < NH) {
+            const int n = N0 + i;
+            const float ag = an[n] * gam[n];
+            rhs[i] = bn[n] * fmaf(-ag, k_hi[e] + k_lo[e], vv[i]);
+            oq[i] = ag * (q_hi[e] + q_lo[e]);
+          }
+        }
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, rhs);
     };
@@ -858,20 +883,28 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
       constexpr int HF = decltype(hfc)::value;
       constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
       constexpr int NL = round_up(SH + NH, LB);
-      float dd[NL], wr[NL];
-#pragma unroll
-      for (int b = 0; b < NL / LB; ++b) {
-        ptx::tmem_ld_w<LB>(tq + Ly::cD2 + B0 + b * LB, dd + b * LB);
-        ptx::tmem_ld_w<LB>(tq + Ly::cD2 + NMAX + B0 + b * LB, wr + b * LB);
-      }
-      ptx::tmem_wait_ld();
+      constexpr int CH = NH > 12 ? 1 : NL / LB;
       float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
       float dl[NH];
 #pragma unroll
-      for (int i = 0; i < NH; ++i) {
-        const int n = N0 + i;
-        if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[i] + wr[SH + i]);
-        dl[i] = cpa[n] * dd[SH + i];
+      for (int c0 = 0; c0 < NL / LB; c0 += CH) {
+        float dd[CH * LB], wr[CH * LB];
+#pragma unroll
+        for (int b = 0; b < CH; ++b) {
+          const int cb = B0 + (c0 + b) * LB;
+          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + cb, dd + b * LB);
+          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + NMAX + cb, wr + b * LB);
+        }
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < CH * LB; ++e) {
+          const int i = c0 * LB + e - SH;  // node N0 + i
+          if (i >= 0 && i < NH) {
+            const int n = N0 + i;
+            if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[i] + wr[e]);
+            dl[i] = cpa[n] * dd[e];
+          }
+        }
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, dl);
     };
@@ -954,7 +987,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTcTmemCols);
+    ptx::tmem_dealloc(tmem, TcRes<NMAX>::tmem_cols);
   }
 }
 

@@ -26,13 +26,14 @@ constexpr int kPrepThreads = 256;
 // Tree tables of one request in the new labels (the accepted path, root
 // first, takes labels 0..P-1; the other nodes follow in input order, so
 // parents still precede children), built by one warp: lane i holds input
-// node i (N <= NMAX <= 32), ancestor walks are shuffles.  Parent indices
-// that break the tree rules (the step kernel reports such a batch) are
-// clamped so that no index leaves its table.
+// nodes i and i + 32 (N <= NMAX <= 64), ancestor walks are shuffles.
+// Parent indices that break the tree rules (the step kernel reports such a
+// batch) are clamped so that no index leaves its table.
 template <int NMAX>
 __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t *par_b,
                                   unsigned char *tb) {
-  static_assert(NMAX <= 32, "one node per lane");
+  constexpr int S = (NMAX + 31) / 32;  // nodes per lane
+  static_assert(S <= 2, "at most two nodes per lane");
   using TL = TabLayout<NMAX>;
   constexpr unsigned FULL = 0xffffffffu;
   unsigned char *pj = tb + TL::pj, *pn = tb + TL::pn, *ln = tb + TL::ln;
@@ -47,48 +48,97 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
   int *corder = reinterpret_cast<int *>(tb + TL::corder);
   int *crow = reinterpret_cast<int *>(tb + TL::crow);
   int *meta = reinterpret_cast<int *>(tb + TL::meta);
-  const bool real = lane < N;
-  int p = real ? par_b[lane] : -1;
-  if (!(p >= 0 && p < lane)) p = -1;
+  // value v[] of node m (held by lane m & 31, slot m >> 5); warp-collective,
+  // m in [0, 32 S)
+  auto at = [&](const int (&v)[S], int m) {
+    int r = __shfl_sync(FULL, v[0], m & 31);
+    if constexpr (S > 1) {
+      const int r1 = __shfl_sync(FULL, v[1], m & 31);
+      if (m >= 32) r = r1;
+    }
+    return r;
+  };
+  auto ballot64 = [&](const bool (&c)[S]) {
+    unsigned long long m = __ballot_sync(FULL, c[0]);
+    if constexpr (S > 1) m |= (unsigned long long)__ballot_sync(FULL, c[1]) << 32;
+    return m;
+  };
+  int p[S];
+  bool real[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    real[s] = i < N;
+    p[s] = real[s] ? par_b[i] : -1;
+    if (!(p[s] >= 0 && p[s] < i)) p[s] = -1;
+  }
   if (!(acc >= 0 && acc < N)) acc = 0;
   // depth: number of strict ancestors
-  int d = 0;
+  int d[S];
   {
-    int m = p;
+    int m[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      d[s] = 0;
+      m[s] = p[s];
+    }
 #pragma unroll 1
-    for (int it = 0; it < NMAX && __any_sync(FULL, m >= 0); ++it) {
-      const int up = __shfl_sync(FULL, p, m >= 0 ? m : 0);
-      if (m >= 0) {
-        ++d;
-        m = up;
+    for (int it = 0; it < NMAX; ++it) {
+      bool any = false;
+#pragma unroll
+      for (int s = 0; s < S; ++s) any |= m[s] >= 0;
+      if (!__any_sync(FULL, any)) break;
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        const int up = at(p, m[s] >= 0 ? m[s] : 0);
+        if (m[s] >= 0) {
+          ++d[s];
+          m[s] = up;
+        }
       }
     }
   }
   // the accepted path (acc and its ancestors): the same walk in every lane
-  bool onp = false;
+  bool onp[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) onp[s] = false;
   {
     int c = acc;
 #pragma unroll 1
     for (int it = 0; it <= NMAX && c >= 0; ++it) {
-      onp |= lane == c;
-      c = __shfl_sync(FULL, p, c);
+#pragma unroll
+      for (int s = 0; s < S; ++s) onp[s] |= lane + 32 * s == c;
+      c = at(p, c);
     }
   }
-  const unsigned pathm = __ballot_sync(FULL, onp && real);
-  const unsigned restm = __ballot_sync(FULL, !onp && real);
-  const int P = __popc(pathm);
+  bool cp[S], cr[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    cp[s] = onp[s] && real[s];
+    cr[s] = !onp[s] && real[s];
+  }
+  const unsigned long long pathm = ballot64(cp), restm = ballot64(cr);
+  const int P = __popcll(pathm);
   // new label: depth on the path, else after the path in input order
-  const int nlab = onp ? d : P + __popc(restm & ((1u << lane) - 1u));
-  const int newp_src = __shfl_sync(FULL, nlab, p >= 0 ? p : 0);
+  int nlab[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    nlab[s] = onp[s] ? d[s] : P + __popcll(restm & ((1ull << i) - 1ull));
+  }
+  int newp_src[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) newp_src[s] = at(nlab, p[s] >= 0 ? p[s] : 0);
   // conv window rows (input labels) of each node: itself, then ancestors,
   // then cached rows (-1 - row); taps j >= K and padding nodes read row 0
-  int wj[4];
-  {
-    int m = real ? lane : -2, past = 0;
+  int wj[S][4];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    int m = real[s] ? lane + 32 * s : -2, past = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       int w = 0;
-      if (real && j < K) {
+      if (real[s] && j < K) {
         if (m >= 0) {
           w = m;
         } else {
@@ -96,28 +146,33 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
           w = -1 - (K - 1 - past);
         }
       }
-      wj[j] = w;
-      const int up = __shfl_sync(FULL, p, m >= 0 ? m : 0);
-      if (real && j < K && m >= 0) m = up;
+      wj[s][j] = w;
+      const int up = at(p, m >= 0 ? m : 0);
+      if (real[s] && j < K && m >= 0) m = up;
     }
   }
-  if (real) {
-    n2o[nlab] = lane;
-    o2n[lane] = nlab;
-    par[nlab] = p >= 0 ? newp_src : -1;
-    dep[nlab] = d;
-    *reinterpret_cast<int4 *>(win + 4 * nlab) = make_int4(wj[0], wj[1], wj[2], wj[3]);
-  } else if (lane < NMAX) {
-    n2o[lane] = 0;
-    o2n[lane] = -1;
-    par[lane] = -1;
-    dep[lane] = 0;
-    *reinterpret_cast<int4 *>(win + 4 * lane) = make_int4(0, 0, 0, 0);
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    if (real[s]) {
+      n2o[nlab[s]] = i;
+      o2n[i] = nlab[s];
+      par[nlab[s]] = p[s] >= 0 ? newp_src[s] : -1;
+      dep[nlab[s]] = d[s];
+      *reinterpret_cast<int4 *>(win + 4 * nlab[s]) =
+          make_int4(wj[s][0], wj[s][1], wj[s][2], wj[s][3]);
+    } else if (i < NMAX) {
+      n2o[i] = 0;
+      o2n[i] = -1;
+      par[i] = -1;
+      dep[i] = 0;
+      *reinterpret_cast<int4 *>(win + 4 * i) = make_int4(0, 0, 0, 0);
+    }
   }
   // new-window sources of the persist: row rr takes the (K-2-rr)-th
   // ancestor of acc, or old cache row depth(acc)+1+rr where the path is short
   {
-    const int da = __shfl_sync(FULL, d, acc);
+    const int da = at(d, acc);
     int src[3] = {0, 0, 0};
     int m = acc;
 #pragma unroll
@@ -125,7 +180,7 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
 #pragma unroll
       for (int rr = 0; rr < 3; ++rr)
         if (rr < K - 1 && K - 2 - rr == step && step <= da) src[rr] = m;
-      m = __shfl_sync(FULL, p, m >= 0 ? m : 0);
+      m = at(p, m >= 0 ? m : 0);
     }
 #pragma unroll
     for (int rr = 0; rr < 3; ++rr)
@@ -135,56 +190,78 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
     }
   }
   __syncwarp();
-  // parent-path and lane offsets in the new labels (lane = new label)
-  const int dl = lane < N ? dep[lane] : 0;
-  const int pl = lane < N ? par[lane] : -1;
-  int s1 = dl, s2 = lane < N ? dl + 1 : 0;
+  // parent-path and lane offsets in the new labels (node i = lane + 32 s is
+  // now a new label): exclusive prefix sums of depth and depth + 1
+  int dl[S], pl[S], e1[S], e2[S];
+  int carry1 = 0, carry2 = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t1 = __shfl_up_sync(FULL, s1, o), t2 = __shfl_up_sync(FULL, s2, o);
-    if (lane >= o) {
-      s1 += t1;
-      s2 += t2;
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    dl[s] = i < N ? dep[i] : 0;
+    pl[s] = i < N ? par[i] : -1;
+    const int v2 = i < N ? dl[s] + 1 : 0;
+    int s1 = dl[s], s2 = v2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t1 = __shfl_up_sync(FULL, s1, o), t2 = __shfl_up_sync(FULL, s2, o);
+      if (lane >= o) {
+        s1 += t1;
+        s2 += t2;
+      }
+    }
+    e1[s] = carry1 + s1 - dl[s];
+    e2[s] = carry2 + s2 - v2;
+    carry1 += __shfl_sync(FULL, s1, 31);
+    carry2 += __shfl_sync(FULL, s2, 31);
+  }
+  // conv order: nodes whose window lies inside the tree (depth >= K-1) first
+  bool ins[S], outs[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    ins[s] = i < N && dl[s] >= K - 1;
+    outs[s] = i < N && !ins[s];
+  }
+  const unsigned long long insm = ballot64(ins), outm = ballot64(outs);
+  const int n_inside = __popcll(insm);
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    const unsigned long long lt = (1ull << i) - 1ull;
+    if (i < N)
+      corder[ins[s] ? __popcll(insm & lt) : n_inside + __popcll(outm & lt)] = i;
+    else if (i < NMAX)
+      corder[i] = 0;
+    if (i <= NMAX) {
+      off[i] = e1[s];
+      off2[i] = e2[s];
     }
   }
-  const int e1 = s1 - dl, e2 = s2 - (lane < N ? dl + 1 : 0);  // exclusive prefix
-  // conv order: nodes whose window lies inside the tree (depth >= K-1) first
-  const bool inside = lane < N && dl >= K - 1;
-  const unsigned lt = (1u << lane) - 1u;
-  const unsigned insm = __ballot_sync(FULL, inside);
-  const unsigned outm = __ballot_sync(FULL, lane < N && !inside);
-  const int n_inside = __popc(insm);
-  if (lane < N)
-    corder[inside ? __popc(insm & lt) : n_inside + __popc(outm & lt)] = lane;
-  else if (lane < NMAX)
-    corder[lane] = 0;
-  if (lane <= NMAX) {
-    off[lane] = e1;
-    off2[lane] = e2;
-  }
-  if (lane == N) {
+  if (lane == 0) {
     meta[0] = P;
-    meta[1] = e2;
-    meta[2] = e1;
+    meta[1] = carry2;  // lanes
+    meta[2] = carry1;  // pairs
     meta[3] = n_inside;
   }
   // pairs (node, strict ancestor) and lanes (node, ancestor-or-self)
-  {
-    int j = pl, t = 0;
-    if (lane < N) {
-      ln[e2] = (unsigned char)lane;
-      lofs[e2] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, lane, lane);
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int i = lane + 32 * s;
+    int j = pl[s], tt = 0;
+    if (i < N) {
+      ln[e2[s]] = (unsigned char)i;
+      lofs[e2[s]] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, i, i);
     }
 #pragma unroll 1
     for (int it = 0; it < NMAX && __any_sync(FULL, j >= 0); ++it) {
-      if (lane < N && j >= 0) {
-        pj[e1 + t] = (unsigned char)j;
-        pn[e1 + t] = (unsigned char)lane;
-        ln[e2 + t + 1] = (unsigned char)lane;
-        lofs[e2 + t + 1] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, lane, j);
-        ++t;
+      if (i < N && j >= 0) {
+        pj[e1[s] + tt] = (unsigned char)j;
+        pn[e1[s] + tt] = (unsigned char)i;
+        ln[e2[s] + tt + 1] = (unsigned char)i;
+        lofs[e2[s] + tt + 1] = (uint16_t)plain_bf16(TcLayout<NMAX>::KP, i, j);
+        ++tt;
       }
-      const int up = __shfl_sync(FULL, pl, j >= 0 ? j : 0);
+      const int up = at(pl, j >= 0 ? j : 0);
       if (j >= 0) j = up;
     }
   }
@@ -192,7 +269,7 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
 }
 
 template <int NMAX>
-__global__ void __launch_bounds__(kPrepThreads, 4)
+__global__ void __launch_bounds__(kPrepThreads, TcRes<NMAX>::prep_ctas)
     gdn_qk_prep_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using PL = PrepLayout<NMAX>;
@@ -201,6 +278,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   using GL = GramLayout<NMAX>;
   using HL = HeadLayout<NMAX>;
   constexpr int NT = kPrepThreads, NC = Ly::NC, R1 = Ly::R1, TP = Ly::TP, NP = PL::NP;
+  constexpr int kPrepHeads = PL::kPrepHeads;
   const StepArgs &A = T.s;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *sq = smem + PL::sq, *sk = smem + PL::sk;
