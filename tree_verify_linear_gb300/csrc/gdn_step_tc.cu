@@ -89,7 +89,7 @@ int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
     if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem) !=
         cudaSuccess)
       return LBX_ECUDA;
-    prep<<<A.L * A.Bq * A.Hk, kPrepThreads, psmem, st>>>(maps, T);
+    prep<<<A.L * A.Bq * A.Hk, TcRes<NMAX>::prep_threads, psmem, st>>>(maps, T);
     if (cudaGetLastError() != cudaSuccess) return LBX_ECUDA;
   }
   auto kern = gdn_step_tc_kernel<NMAX>;

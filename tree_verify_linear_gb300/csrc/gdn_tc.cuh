@@ -65,8 +65,9 @@ __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / 
 // Resources of the tree step by node capacity: up to 24 nodes two CTAs share
 // an SM (256 TMEM columns and at most 113 KB of shared memory each); larger
 // capacities (up to 64) take one CTA per SM with all 512 TMEM columns.  The
-// prep kernel handles kPrepHeads value heads at a time (its per-head scratch
-// grows with NMAX^2).
+// prep kernel handles prep_heads value heads at a time (its per-head scratch
+// grows with NMAX^2); at the large capacities its shared memory allows one
+// CTA per SM, which then runs 16 warps.
 template <int NMAX>
 struct TcRes {
   static constexpr int ctas = NMAX <= 24 ? 2 : 1;
@@ -74,6 +75,7 @@ struct TcRes {
   static constexpr int max_smem = NMAX <= 24 ? 113 * 1024 : 227 * 1024;
   static constexpr int prep_ctas = NMAX <= 24 ? 4 : 1;
   static constexpr int prep_heads = NMAX <= 24 ? 4 : 2;
+  static constexpr int prep_threads = NMAX <= 24 ? 256 : 512;
 };
 
 // Staged conv inputs of one 128-channel block for N nodes: raw inputs

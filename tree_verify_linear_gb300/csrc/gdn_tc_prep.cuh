@@ -21,7 +21,6 @@
 
 namespace lbx {
 
-constexpr int kPrepThreads = 256;
 
 // Tree tables of one request in the new labels (the accepted path, root
 // first, takes labels 0..P-1; the other nodes follow in input order, so
@@ -269,7 +268,7 @@ __device__ void build_tables_warp(int lane, int N, int K, int acc, const int32_t
 }
 
 template <int NMAX>
-__global__ void __launch_bounds__(kPrepThreads, TcRes<NMAX>::prep_ctas)
+__global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_ctas)
     gdn_qk_prep_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
   using Ly = TcLayout<NMAX>;
   using PL = PrepLayout<NMAX>;
@@ -277,6 +276,7 @@ __global__ void __launch_bounds__(kPrepThreads, TcRes<NMAX>::prep_ctas)
   using TL = TabLayout<NMAX>;
   using GL = GramLayout<NMAX>;
   using HL = HeadLayout<NMAX>;
+  constexpr int kPrepThreads = TcRes<NMAX>::prep_threads;
   constexpr int NT = kPrepThreads, NC = Ly::NC, R1 = Ly::R1, TP = Ly::TP, NP = PL::NP;
   constexpr int kPrepHeads = PL::kPrepHeads;
   const StepArgs &A = T.s;
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kPrepThreads, TcRes<NMAX>::prep_ctas)
     *reinterpret_cast<uint4 *>(img + sw128_bf16(R1, NC + brow, c8 * 8)) =
         make_uint4(wl[0], wl[1], wl[2], wl[3]);
   }
-  {
+  if (tid < 2 * kTcD) {
     // new conv window of the key head's q (threads 0..127) and k (128..255)
     // channels, from the staged old window and inputs
     const int which = tid >> 7, c = tid & (kTcD - 1);
