@@ -56,7 +56,7 @@ def lib():
             for name in ("lbxo_check_tree", "lbxo_conv_lb", "lbxo_tree_conv",
                          "lbxo_deltanet_head", "lbxo_persist_conv_lb", "lbxo_verify_heads",
                          "lbxo_tree_deltanet", "lbxo_tree_persist", "lbxo_accept_walk",
-                         "lbxo_ddtree_build"):
+                         "lbxo_ddtree_build", "lbxo_tree_attention"):
                 getattr(_lib, name).restype = ctypes.c_int
         return _lib
 
@@ -238,3 +238,25 @@ def ddtree_build(logp: np.ndarray, tok: np.ndarray, root_tok: np.ndarray, B: int
                                    ctypes.c_int(B), _p(lp), _p(tk), _p(rt), _p(par), _p(tn),
                                    _p(dp), _p(sc), _p(nn)), "lbxo_ddtree_build")
     return par, tn, dp, sc, nn
+
+
+def tree_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, k_tree: np.ndarray,
+                   v_tree: np.ndarray, ctx_len: np.ndarray, parent: np.ndarray,
+                   scale: float) -> np.ndarray:
+    """Tree-masked attention of the full-attention layers (see lbx_oracle.c).
+
+    q uint16 (bf16 bits) [L][Bq][N][Hq][dh]; k_cache, v_cache [L][Bq][T][Hkv][dh];
+    k_tree, v_tree [L][Bq][N][Hkv][dh]; ctx_len int32 [Bq]; parent int32
+    [Bq][N].  Returns o float64 [L][Bq][N][Hq][dh]."""
+    L, Bq, N, Hq, dh = q.shape
+    T, Hkv = k_cache.shape[2], k_cache.shape[3]
+    arrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in (q, k_cache, v_cache, k_tree, v_tree)]
+    cl = np.ascontiguousarray(ctx_len, dtype=np.int32).reshape(Bq)
+    pa = np.ascontiguousarray(parent, dtype=np.int32).reshape(Bq, N)
+    o = np.zeros((L, Bq, N, Hq, dh), dtype=np.float64)
+    _check(lib().lbxo_tree_attention(ctypes.c_int(L), ctypes.c_int(Bq), ctypes.c_int(N),
+                                     ctypes.c_int(Hq), ctypes.c_int(Hkv), ctypes.c_int(dh),
+                                     ctypes.c_int(T), _p(cl), ctypes.c_double(scale),
+                                     *[_p(a) for a in arrs], _p(pa), _p(o)),
+           "lbxo_tree_attention")
+    return o

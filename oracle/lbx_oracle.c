@@ -658,3 +658,82 @@ int lbxo_ddtree_build(int Bq, int D, int K, int B, const float *logp, const int3
   free(slot);
   return LBXO_OK;
 }
+
+/* ---- Tree-masked attention of the full-attention layers ---------------------
+ *
+ * Sources: Lucebox hub README -- DDTree verifies the whole draft tree in one
+ * target forward ("Algorithms used": a tree-structured verify), and the
+ * target is a hybrid whose full-attention layers keep a KV cache (flags
+ * "--max-ctx N", the KV cache size, and "--fa-window N", default 0 = full
+ * attention; a finite window drops the system prompt from the full-attention
+ * layers).  The pages print no formula; the plain reading taken:
+ *   - in the verify forward draft node n sits one position after its parent,
+ *     so its query sees the request's cached context (positions
+ *     0..ctx_len[b]-1) and the tree nodes on its own root path (its
+ *     ancestors and itself), nothing else (full attention, no window);
+ *   - query head hq reads KV head hq / (Hq/Hkv) (contiguous GQA groups);
+ *   - o[n][hq] = sum_j softmax_j(scale * q.k_j) v_j over that key set.
+ * Layers are a batch dimension sharing the tree and the context lengths:
+ * q [L][Bq][N][Hq][dh], k_cache and v_cache [L][Bq][T][Hkv][dh], k_tree and
+ * v_tree [L][Bq][N][Hkv][dh] (bf16 bit patterns); ctx_len [Bq] in 0..T,
+ * parent [Bq][N]; o [L][Bq][N][Hq][dh] double out.
+ */
+int lbxo_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh, int T,
+                        const int32_t *ctx_len, double scale, const uint16_t *q,
+                        const uint16_t *k_cache, const uint16_t *v_cache, const uint16_t *k_tree,
+                        const uint16_t *v_tree, const int32_t *parent, double *o) {
+  if (L < 1 || Bq < 1 || N < 1 || Hq < 1 || Hkv < 1 || dh < 1 || T < 0 || Hq % Hkv) return LBXO_EINVAL;
+  for (int bb = 0; bb < Bq; ++bb) {
+    if (ctx_len[bb] < 0 || ctx_len[bb] > T) return LBXO_EINVAL;
+    if (lbxo_check_tree(parent + (size_t)bb * N, N) != LBXO_OK) return LBXO_ETREE;
+  }
+  const int G = Hq / Hkv;
+  int *path = malloc((size_t)N * sizeof *path);
+  double *s = malloc(((size_t)T + N) * sizeof *s);
+  if (!path || !s) {
+    free(path);
+    free(s);
+    return LBXO_ENOMEM;
+  }
+  for (int l = 0; l < L; ++l)
+    for (int bb = 0; bb < Bq; ++bb) {
+      const size_t lb = (size_t)l * Bq + bb;
+      const int C = ctx_len[bb];
+      const int32_t *par = parent + (size_t)bb * N;
+      for (int n = 0; n < N; ++n) {
+        int P = 0; /* the tree keys of node n: itself and its ancestors */
+        for (int j = n; j >= 0; j = par[j]) path[P++] = j;
+        for (int hq = 0; hq < Hq; ++hq) {
+          const int g = hq / G;
+          const uint16_t *qv = q + ((lb * N + n) * Hq + hq) * (size_t)dh;
+          /* scores of the context keys, then of the path keys */
+          for (int t = 0; t < C + P; ++t) {
+            const uint16_t *kv = t < C ? k_cache + ((lb * T + t) * Hkv + g) * (size_t)dh
+                                       : k_tree + ((lb * N + path[t - C]) * Hkv + g) * (size_t)dh;
+            double dot = 0.0;
+            for (int i = 0; i < dh; ++i) dot += bf16_to_double(qv[i]) * bf16_to_double(kv[i]);
+            s[t] = scale * dot;
+          }
+          double mx = s[0];
+          for (int t = 1; t < C + P; ++t)
+            if (s[t] > mx) mx = s[t];
+          double sum = 0.0;
+          for (int t = 0; t < C + P; ++t) {
+            s[t] = exp(s[t] - mx);
+            sum += s[t];
+          }
+          double *out = o + ((lb * N + n) * Hq + hq) * (size_t)dh;
+          for (int i = 0; i < dh; ++i) out[i] = 0.0;
+          for (int t = 0; t < C + P; ++t) {
+            const uint16_t *vv = t < C ? v_cache + ((lb * T + t) * Hkv + g) * (size_t)dh
+                                       : v_tree + ((lb * N + path[t - C]) * Hkv + g) * (size_t)dh;
+            const double p = s[t] / sum;
+            for (int i = 0; i < dh; ++i) out[i] += p * bf16_to_double(vv[i]);
+          }
+        }
+      }
+    }
+  free(path);
+  free(s);
+  return LBXO_OK;
+}

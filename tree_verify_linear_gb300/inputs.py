@@ -266,3 +266,79 @@ def make_draft_topk(Bq: int, D: int, K: int, V: int, seed: int) -> dict:
             tok[b, d] = rng.choice(V, size=K, replace=False)
     root = rng.integers(0, V, size=Bq).astype(np.int32)
     return {"logp": logp, "tok": tok, "root_tok": root}
+
+
+# ---- tree-masked attention inputs -------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Shape of the tree-masked attention of the full-attention layers in one
+    verify step.  The pages give no attention shapes; the 27B-class layer is
+    taken as 24 query heads over 4 KV heads of dimension 256 (GQA groups of 6)."""
+
+    name: str
+    L: int            # full-attention layers (a batch dimension)
+    Bq: int           # requests
+    N: int            # draft-tree nodes
+    Hq: int           # query heads
+    Hkv: int          # KV heads
+    dh: int           # head dimension
+    T: int            # KV-cache capacity (positions)
+    ctx: str = "full"  # full: ctx_len = T; ragged: uniform on [T/2, T], plus one 0 when Bq > 2
+    tree: str = "ddtree"
+    max_children: Optional[int] = None
+    seed: int = 2000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.dh))
+
+    def replace(self, **kw) -> "AttnWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+ATTN_WORKLOADS = {
+    "attn_tiny": AttnWorkload("attn_tiny", L=1, Bq=3, N=8, Hq=4, Hkv=2, dh=256, T=40,
+                              ctx="ragged", tree="uniform", seed=2001),
+    "attn27b": AttnWorkload("attn27b", L=16, Bq=1, N=22, Hq=24, Hkv=4, dh=256, T=4096,
+                            seed=2002),
+    "attn27b_serve": AttnWorkload("attn27b_serve", L=16, Bq=5, N=22, Hq=24, Hkv=4, dh=256,
+                                  T=8192, ctx="ragged", seed=2003),
+}
+
+
+def make_attn_inputs(w: AttnWorkload, seed: Optional[int] = None) -> dict:
+    """Seeded inputs of the tree-masked attention: q, k, v ~ N(0, 1) rounded
+    to bf16 (the configs' input distribution), as bit patterns; DDTree-shaped
+    (or uniform / chain) trees as for the verify step; context lengths.
+
+      q        uint16 [L][Bq][N][Hq][dh]
+      k_cache  uint16 [L][Bq][T][Hkv][dh]    (v_cache alike)
+      k_tree   uint16 [L][Bq][N][Hkv][dh]    (v_tree alike)
+      ctx_len  int32  [Bq]
+      parent   int32  [Bq][N]
+    """
+    s = w.seed if seed is None else seed
+    rng = _rng(s, 99)
+    L, Bq, N = w.L, w.Bq, w.N
+
+    def normal(*shape):
+        return bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+    q = normal(L, Bq, N, w.Hq, w.dh)
+    k_cache = normal(L, Bq, w.T, w.Hkv, w.dh)
+    v_cache = normal(L, Bq, w.T, w.Hkv, w.dh)
+    k_tree = normal(L, Bq, N, w.Hkv, w.dh)
+    v_tree = normal(L, Bq, N, w.Hkv, w.dh)
+    if w.ctx == "full":
+        ctx_len = np.full(Bq, w.T, dtype=np.int32)
+    elif w.ctx == "ragged":
+        ctx_len = rng.integers(w.T // 2, w.T + 1, size=Bq).astype(np.int32)
+        if Bq > 2:
+            ctx_len[1] = 0
+    else:
+        raise ValueError(f"unknown context kind {w.ctx!r}")
+    parent = np.stack([make_tree(rng, N, w.tree, max_children=w.max_children)
+                       for _ in range(Bq)]).astype(np.int32)
+    return dict(q=q, k_cache=k_cache, v_cache=v_cache, k_tree=k_tree, v_tree=v_tree,
+                ctx_len=ctx_len, parent=parent)
