@@ -68,6 +68,8 @@ extern "C" {
 #define LBX_ACCEPT_MAX_NODES 4096 /* lbx_accept_walk: N <= 4096 nodes         */
 #define LBX_DDTREE_MAX_K 8        /* lbx_ddtree_build: top-K, 1 <= K <= 8       */
 #define LBX_DDTREE_MAX_DEPTH 64   /* lbx_ddtree_build: draft positions D <= 64  */
+#define LBX_ATTN_HEAD_DIM 256     /* lbx_tree_attention: head dimension         */
+#define LBX_ATTN_MAX_NODES 64     /* lbx_tree_attention: N <= 64 tree nodes     */
 
 /* Modes of lbx_verify_step. */
 #define LBX_MODE_AUTO 0    /* tree if N <= LBX_MAX_TREE_NODES, else chunked     */
@@ -280,6 +282,47 @@ int lbx_ddtree_build(int Bq, int D, int K, int B, const float *logp, const int32
                      const int32_t *root_tok, int32_t *parent_out, int32_t *token_out,
                      int32_t *depth_out, float *score_out, int32_t *n_nodes_out,
                      cudaStream_t stream);
+
+/* Bytes of workspace lbx_tree_attention needs for these shapes (0 if they
+ * are not supported).  It must be zero-filled once before its first use;
+ * every call that runs to completion leaves its counters at zero again; two
+ * calls that run at the same time must not share a workspace. */
+size_t lbx_attn_workspace_size(int L, int Bq, int N, int Hq, int Hkv, int dh, int T);
+
+/*
+ * Tree-masked attention of the hybrid target's full-attention layers in the
+ * verify forward (Lucebox hub README: DDTree verifies the whole draft tree in
+ * one target forward, "Algorithms used"; the full-attention layers keep a KV
+ * cache, "--max-ctx N", and attend to all of it by default, "--fa-window N"
+ * = 0).  Draft node n sits one position after its parent, so its query sees
+ * the request's cached context and the tree nodes on its own root path
+ * (its ancestors and itself):
+ *     o[l][b][n][hq] = sum_j softmax_j(scale * q[l][b][n][hq] . k_j) v_j,
+ * over j in { cache positions 0 .. ctx_len[b]-1 } u { tree nodes on the path
+ * root -> n }, with KV head g = hq / (Hq/Hkv) (contiguous GQA groups).
+ * Layers are a batch dimension sharing the tree and the context lengths.
+ *   q        [L][Bq][N][Hq][dh]   bf16
+ *   k_cache, v_cache [L][Bq][T][Hkv][dh] bf16 (T = capacity; may be NULL
+ *            when T == 0); positions at or past ctx_len[b] are never used
+ *   k_tree, v_tree   [L][Bq][N][Hkv][dh] bf16: the tree nodes' own keys and
+ *            values (already projected and position-encoded by the caller)
+ *   ctx_len  [Bq] int32 in 0..T;  parent [Bq][N] int32 (the draft tree)
+ *   o        [L][Bq][N][Hq][dh]   fp32 out
+ *   scale    > 0, finite (1/sqrt(dh) for plain scaled dot-product attention)
+ * dh must be LBX_ATTN_HEAD_DIM and 1 <= N <= LBX_ATTN_MAX_NODES; Hq % Hkv ==
+ * 0.  Computed on the tensor cores: S = Q K^T per key block and O += P V with
+ * bf16 operands (P split into hi + lo) and fp32 accumulation, softmax in
+ * fp32.  Device pointers owned by the caller (bf16 arrays and o 16-byte
+ * aligned); asynchronous on `stream`.  Returns LBX_EINVAL for unsupported
+ * shapes, NULL or misaligned pointers or a short workspace, LBX_ECUDA if the
+ * launch fails; an invalid tree or a ctx_len outside 0..T is reported as
+ * LBX_ETREE through d_status (nullable) and nothing is written.
+ */
+int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh, int T, float scale,
+                       const int32_t *ctx_len, const int32_t *parent, const uint16_t *q,
+                       const uint16_t *k_cache, const uint16_t *v_cache, const uint16_t *k_tree,
+                       const uint16_t *v_tree, float *o, void *workspace, size_t workspace_bytes,
+                       int32_t *d_status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -27,10 +27,12 @@ LBX_MODE_AUTO, LBX_MODE_TREE, LBX_MODE_CHUNKED, LBX_MODE_TREE_CUDA_CORES = 0, 1,
 # Every function the header declares, in header order.
 EXPORTS = ("lbx_strerror", "lbx_workspace_size", "lbx_tree_conv", "lbx_tree_deltanet",
            "lbx_tree_persist", "lbx_verify_step", "lbx_verify_step_noalloc",
-           "lbx_accept_workspace_size", "lbx_accept_walk", "lbx_ddtree_build")
+           "lbx_accept_workspace_size", "lbx_accept_walk", "lbx_ddtree_build",
+           "lbx_attn_workspace_size", "lbx_tree_attention")
 LBX_ACCEPT_MAX_NODES = 4096
 LBX_DDTREE_MAX_K, LBX_DDTREE_MAX_DEPTH = 8, 64
 LBX_NOALLOC_MAX_GROUPS = 65536
+LBX_ATTN_HEAD_DIM, LBX_ATTN_MAX_NODES = 256, 64
 
 
 class LbxError(RuntimeError):
@@ -77,6 +79,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lbx_accept_walk.argtypes = [i32, i32, i32] + [vp] * 6 + [vp, ctypes.c_size_t, vp, vp]
         lib.lbx_ddtree_build.restype = i32
         lib.lbx_ddtree_build.argtypes = [i32, i32, i32, i32] + [vp] * 9
+        lib.lbx_attn_workspace_size.restype = ctypes.c_size_t
+        lib.lbx_attn_workspace_size.argtypes = [i32] * 7
+        lib.lbx_tree_attention.restype = i32
+        lib.lbx_tree_attention.argtypes = ([i32] * 7 + [ctypes.c_float] + [vp] * 8
+                                           + [vp, ctypes.c_size_t, vp, vp])
         _lib = lib
     return _lib
 
@@ -226,3 +233,31 @@ def lbx_ddtree_build(logp, tok, root_tok, B, parent_out, token_out, n_nodes_out,
         _i32(parent_out, "parent_out"), _i32(token_out, "token_out"),
         _i32(depth_out, "depth_out"), _f32(score_out, "score_out"),
         _i32(n_nodes_out, "n_nodes_out"), _stream(stream)))
+
+
+def lbx_attn_workspace_size(L: int, Bq: int, N: int, Hq: int, Hkv: int, dh: int, T: int) -> int:
+    return int(load().lbx_attn_workspace_size(L, Bq, N, Hq, Hkv, dh, T))
+
+
+def new_attn_workspace(L, Bq, N, Hq, Hkv, dh, T, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of lbx_attn_workspace_size(...) bytes."""
+    n = lbx_attn_workspace_size(L, Bq, N, Hq, Hkv, dh, T)
+    if n == 0:
+        raise LbxError("lbx_attn_workspace_size", LBX_EINVAL)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def lbx_tree_attention(scale, ctx_len, parent, q, k_cache, v_cache, k_tree, v_tree, o, workspace,
+                       d_status=None, stream=None):
+    """Tree-masked attention of the full-attention layers: q bf16
+    [L][Bq][N][Hq][dh], k_cache / v_cache [L][Bq][T][Hkv][dh], k_tree / v_tree
+    [L][Bq][N][Hkv][dh], o float32 like q; shapes are read from the tensors."""
+    L, Bq, N, Hq, dh = q.shape
+    T, Hkv = k_cache.shape[2], k_cache.shape[3]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("lbx_tree_attention", load().lbx_tree_attention(
+        L, Bq, N, Hq, Hkv, dh, T, float(scale), _i32(ctx_len, "ctx_len"), _i32(parent, "parent"),
+        _bf(q, "q"), _bf(k_cache, "k_cache") if T > 0 else None,
+        _bf(v_cache, "v_cache") if T > 0 else None, _bf(k_tree, "k_tree"), _bf(v_tree, "v_tree"),
+        _f32(o, "o"), _ptr(workspace, None, "workspace"), ws_bytes, _i32(d_status, "d_status"),
+        _stream(stream)))
