@@ -11,10 +11,11 @@ with the step's inputs copied from pinned host memory and o copied back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lbx|reference]
-                       [--workload NAME] [--op verify|accept|ddtree]
+                       [--workload NAME] [--op verify|accept|ddtree|attn]
 `--op accept` times lbx_accept_walk (verify argmax + greedy acceptance walk)
-on a 5-request serving batch instead, `--op ddtree` lbx_ddtree_build (each
-a separate JSON line of its own).
+on a 5-request serving batch instead, `--op ddtree` lbx_ddtree_build, `--op
+attn` lbx_tree_attention on --attn-workload (each a separate JSON line of its
+own).
 Under torchrun each rank runs an independent replica (the path needs no
 exchange between GPUs); value is the sum over ranks of the work done divided
 by the slowest rank's time.
@@ -571,6 +572,140 @@ def run_ddtree(args):
     print(json.dumps(line))
 
 
+def attn_algorithmic_bytes(w, ctx_len) -> int:
+    """Bytes one tree-attention call must move: each request's cached keys
+    and values up to its context length, q, the tree's keys and values, o
+    (fp32), the context lengths and parent arrays."""
+    kv = int(np.asarray(ctx_len, dtype=np.int64).sum()) * w.L * w.Hkv * w.dh * 2 * 2
+    q = w.L * w.Bq * w.N * w.Hq * w.dh * 2
+    tree = 2 * w.L * w.Bq * w.N * w.Hkv * w.dh * 2
+    o = w.L * w.Bq * w.N * w.Hq * w.dh * 4
+    return kv + q + tree + o + w.Bq * 4 + w.Bq * w.N * 4
+
+
+def run_attn(args):
+    """Times lbx_tree_attention (the full-attention layers of the verify
+    forward) on --attn-workload; the default, attn27b, reads 268 MB of KV
+    cache per call (> L2)."""
+    import torch
+    from tree_verify_linear_gb300 import lbx
+    from tree_verify_linear_gb300.inputs import ATTN_WORKLOADS, make_attn_inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lbx.load()
+    w = ATTN_WORKLOADS[args.attn_workload]
+    inp = make_attn_inputs(w, seed=w.seed + 7919 * rank)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = {k: to_dev(v) for k, v in inp.items()}
+    o = torch.empty((w.L, w.Bq, w.N, w.Hq, w.dh), device=dev)
+    ws = lbx.new_attn_workspace(w.L, w.Bq, w.N, w.Hq, w.Hkv, w.dh, w.T, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        lbx.lbx_tree_attention(w.scale, d["ctx_len"], d["parent"], d["q"], d["k_cache"],
+                               d["v_cache"], d["k_tree"], d["v_tree"], o, ws, status, stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    gpu_id = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid) if uuid else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    us = 1e3 * ms / args.steps
+
+    # end to end: the step's queries, tree keys / values, context lengths and
+    # parents from pinned host memory, o back (the KV cache stays resident)
+    names_in = ("q", "k_tree", "v_tree", "ctx_len", "parent")
+    host = {k: d[k].cpu().pin_memory() for k in names_in}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e():
+        for k in names_in:
+            d[k].copy_(host[k], non_blocking=True)
+        call()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = 1e3 * max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    if rank != 0:
+        return
+    import oracle  # CPU baseline leg only
+    cpu = None
+    if not args.no_cpu_baseline:
+        # one (layer) slice of the call, scaled to the whole call
+        t0 = time.time()
+        sl = {k: (np.ascontiguousarray(v[:1]) if k not in ("ctx_len", "parent") else v)
+              for k, v in inp.items()}
+        oracle.tree_attention(sl["q"], sl["k_cache"], sl["v_cache"], sl["k_tree"], sl["v_tree"],
+                              sl["ctx_len"], sl["parent"], w.scale)
+        dt = time.time() - t0
+        cpu = {"value": 1e6 * dt * w.L, "unit": "us per call", "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of {w.L} (all requests, nodes and heads), timed and scaled "
+                         f"by {w.L}"}
+    peak, peak_kind = read_peaks()
+    alg = attn_algorithmic_bytes(w, inp["ctx_len"])
+    achieved = alg / (us / 1e6) / 1e9
+    line = {
+        "metric": "us per tree-masked attention call", "value": us, "unit": "us per call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.L} full-attention layers, {w.Bq} request(s), "
+                               f"budget-{w.N} tree, Hq={w.Hq}, Hkv={w.Hkv}, dh={w.dh}, "
+                               f"context {w.T} ({w.ctx})",
+                   "L": w.L, "Bq": w.Bq, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh,
+                   "T": w.T, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({alg / 1e6:.1f} MB per call)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes": alg, "kernel": "tree_attn_kernel",
+                     "timed": "whole lbx_tree_attention call"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us per call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -580,19 +715,21 @@ def main():
     ap.add_argument("--workload", default="step27b", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("verify", "accept", "ddtree"), default="verify",
+    ap.add_argument("--op", choices=("verify", "accept", "ddtree", "attn"), default="verify",
                     help="verify: lbx_verify_step on --workload (the headline); accept: "
-                         "lbx_accept_walk on a serving batch; ddtree: lbx_ddtree_build")
+                         "lbx_accept_walk on a serving batch; ddtree: lbx_ddtree_build; "
+                         "attn: lbx_tree_attention on --attn-workload")
+    ap.add_argument("--attn-workload", default="attn27b")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
-    if args.op in ("accept", "ddtree"):
+    if args.op in ("accept", "ddtree", "attn"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               f"--op {args.op} times the library only; its oracle is the "
                               "cpu_baseline field"}))
             return
-        (run_accept if args.op == "accept" else run_ddtree)(args)
+        {"accept": run_accept, "ddtree": run_ddtree, "attn": run_attn}[args.op](args)
         return
     if args.impl == "reference":
         run_reference(args, w)

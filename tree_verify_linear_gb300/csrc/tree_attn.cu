@@ -50,7 +50,6 @@ namespace attn {
 
 constexpr int kDh = LBX_ATTN_HEAD_DIM;  // head dimension (256)
 constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
-constexpr int kThreads = 128;           // one thread per row
 constexpr int kKB = 32;                 // keys per block
 constexpr int kStages = 4;              // K/V blocks in flight
 constexpr int kMaxNodes = LBX_ATTN_MAX_NODES;
@@ -67,7 +66,8 @@ constexpr int kStageBytes = 2 * kKBytes;           // K, then V
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kQBytes;
 constexpr int kSmemAnc = kSmemKV + kStages * kStageBytes;  // uint64 [64]
-constexpr int kSmemMisc = kSmemAnc + kMaxNodes * 8;       // int [16]
+constexpr int kSmemRed = kSmemAnc + kMaxNodes * 8;        // float [2][128]
+constexpr int kSmemMisc = kSmemRed + 2 * kRows * 4;       // int [16]
 constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [8]
 constexpr int kSmemTotal = kSmemBars + 8 * 8;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory");
@@ -144,7 +144,20 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uin
   lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// 2^x on the hardware exponential unit (x <= 0 here; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two threads per row: thread (row r, half hf) handles keys 16 hf .. 16 hf +
+// 15 of every block and columns 128 hf .. 128 hf + 127 of O.  Warps w and w+4
+// share TMEM lane quadrant w & 3.
+constexpr int kHalfKeys = kKB / 2;
+constexpr int kHalfCols = kDh / 2;
+
+__global__ void __launch_bounds__(2 * kRows, 1)
     tree_attn_kernel(const __grid_constant__ Maps maps, const Args A) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -152,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = A.N;
   int *misc = reinterpret_cast<int *>(smem + kSmemMisc);  // [0] TMEM base, [1] last CTA
   uint64_t *anc = reinterpret_cast<uint64_t *>(smem + kSmemAnc);
+  float *red = reinterpret_cast<float *>(smem + kSmemRed);  // [2][kRows] per-half values
   uint64_t *kv_bar = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [4]
   uint64_t *s_bar = kv_bar + 4;                                        // [2]
   uint64_t *o_bar = kv_bar + 6;                                        // [2]
@@ -174,11 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- whole-batch validation (the same verdict in every CTA) ----
   {
     int bad_in = 0;
-    for (int i = tid; i < A.Bq * N; i += kThreads) {
+    for (int i = tid; i < A.Bq * N; i += 2 * kRows) {
       const int n = i % N, p = A.parent[i];
       if (n == 0 ? p != -1 : (p < 0 || p >= n)) bad_in = 1;
     }
-    for (int i = tid; i < A.Bq; i += kThreads)
+    for (int i = tid; i < A.Bq; i += 2 * kRows)
       if (A.ctx_len[i] < 0 || A.ctx_len[i] > A.T) bad_in = 1;
     if (__syncthreads_or(bad_in)) {
       if (tid == 0 && A.status) *A.status = LBX_ETREE;
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Q tile: row r = hl * N + n (head hl of the tile, node n), zero padding rows
   {
     const uint4 *qg = reinterpret_cast<const uint4 *>(A.q);
-    for (int idx = tid; idx < kRows * (kDh / 8); idx += kThreads) {
+    for (int idx = tid; idx < kRows * (kDh / 8); idx += 2 * kRows) {
       const int r = idx / (kDh / 8), c16 = idx % (kDh / 8);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (r < rows) {
@@ -237,11 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
-  const uint32_t tq = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quadrant
+  const int quad = warp & 3, hf = warp >> 2;
+  const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quadrant
 
-  const int r = tid;
+  const int r = quad * 32 + lane;
   const bool real_row = r < rows;
   const int n_row = real_row ? r - (r / N) * N : 0;
+  // tree unit: the ancestor bits of this thread's 16 keys of each block
   const uint64_t my_anc = tree_unit && real_row ? anc[n_row] : 0ull;
 
   const bool lead = tid == 0;
@@ -261,17 +277,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ++n_loads;
   };
+  // descriptors of the Q tile and of stage 0; the others are fixed offsets
+  // (added to the 16-byte address field)
+  const uint64_t qdesc = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemQ));
+  const uint64_t kdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemKV));
+  const uint64_t vdesc0 =
+      ptx::sdesc(ptx::smem_u32(smem + kSmemKV + kKBytes), (uint32_t)kKVAtom, 1024u, 2u);
   // S[j & 1] = Q K_j^T: M = 128, N = 32 keys, K = 256 (16 steps)
   auto mma1 = [&](int j) {
-    const uint32_t qa = ptx::smem_u32(smem + kSmemQ);
-    const uint32_t ka = ptx::smem_u32(smem + kSmemKV + (j & (kStages - 1)) * kStageBytes);
+    const uint64_t kd = kdesc0 + (uint64_t)(((j & (kStages - 1)) * kStageBytes) >> 4);
     constexpr uint32_t idesc = ptx::idesc_bf16(128, kKB);
+    const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKB;
 #pragma unroll
     for (int ks = 0; ks < kDh / 16; ++ks) {
-      const uint32_t ao = (uint32_t)((ks >> 2) * (kRows * 128) + (ks & 3) * 32);
-      const uint32_t bo = (uint32_t)((ks >> 2) * kKVAtom + (ks & 3) * 32);
-      ptx::mma_bf16_ss(tmem + kColS + (uint32_t)(j & 1) * kKB, ptx::sdesc_sw128(qa + ao),
-                       ptx::sdesc_sw128(ka + bo), idesc, ks > 0 ? 1u : 0u);
+      const uint64_t ao = (uint64_t)(((ks >> 2) * (kRows * 128) + (ks & 3) * 32) >> 4);
+      const uint64_t bo = (uint64_t)(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
+      ptx::mma_bf16_ss(d, qdesc + ao, kd + bo, idesc, ks > 0 ? 1u : 0u);
     }
     ptx::mma_commit(&s_bar[j & 1]);
     ++n_mma1;
@@ -279,17 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // O += P_j V_j: A = P (TMEM, hi then lo), B = the V block read MN-major
   // (dh contiguous in 64-column atoms kKVAtom apart, 8-key groups 1024 apart)
   auto mma2 = [&](int j, bool acc) {
-    const uint32_t va =
-        ptx::smem_u32(smem + kSmemKV + (j & (kStages - 1)) * kStageBytes + kKBytes);
+    const uint64_t vd = vdesc0 + (uint64_t)(((j & (kStages - 1)) * kStageBytes) >> 4);
     constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kDh);
-    const uint32_t pc = kColP + (uint32_t)(j & 1) * 32;
+    const uint32_t pc = tmem + kColP + (uint32_t)(j & 1) * 32;
     uint32_t accum = acc ? 1u : 0u;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
       for (int ks = 0; ks < kKB / 16; ++ks) {
-        ptx::mma_bf16_ts(tmem + kColO, tmem + pc + pass * 16 + ks * 8,
-                         ptx::sdesc(va + ks * 2048u, (uint32_t)kKVAtom, 1024u, 2u), idesc, accum);
+        ptx::mma_bf16_ts(tmem + kColO, pc + pass * 16 + ks * 8, vd + (uint64_t)(ks * 2048 >> 4),
+                         idesc, accum);
         accum = 1u;
       }
     ptx::mma_commit(&o_bar[j & 1]);
@@ -303,13 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma1(0);
   }
 
-  float m_run = -INFINITY, l_run = 0.f;  // base-2 running max and sum of this row
+  float m_run = -INFINITY, l_run = 0.f;  // base-2 running max; this half's sum
   for (int i = 0; i < nb; ++i) {
-    // ---- S_i ----
+    // ---- this thread's 16 scores of block i ----
     if (!ptx::mbar_wait(&s_bar[i & 1], (uint32_t)((i >> 1) & 1))) bad = true;
     ptx::tc_fence_after();
-    float sv[32];
-    ptx::tmem_ld32(tq + kColS + (uint32_t)(i & 1) * kKB, sv);
+    float sv[kHalfKeys];
+    ptx::tmem_ld16(tq + kColS + (uint32_t)(i & 1) * kKB + hf * kHalfKeys, sv);
     ptx::tmem_wait_ld();
     // the next block's scores, into the other buffer (read in iteration i-1)
     if (lead && i + 1 < nb) {
@@ -317,32 +337,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad = true;
       mma1(i + 1);
     }
-    // ---- softmax of the block (masked keys weigh zero) ----
-    float s2[32];
-    float mb = -INFINITY;
+    // ---- masked, scaled scores and the block maximum of the row ----
+    const int kb = key0 + i * kKB + hf * kHalfKeys;  // this half's first key
+    float s2[kHalfKeys];
+    if (!tree_unit && kb + kHalfKeys <= kend) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const bool ok = tree_unit ? ((my_anc >> (i * kKB + j)) & 1ull) != 0
-                                : key0 + i * kKB + j < kend;
-      s2[j] = ok ? sv[j] * A.scale_log2 : -INFINITY;
-      mb = fmaxf(mb, s2[j]);
-    }
-    float alpha = 1.f;
-    bool need = false;
-    if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
-      alpha = exp2f(m_run - mb);
-      need = l_run > 0.f;
-      l_run *= alpha;
-      m_run = mb;
-    }
-    float p[32];
-    float ps = 0.f;
+      for (int e = 0; e < kHalfKeys; ++e) s2[e] = sv[e] * A.scale_log2;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      p[j] = s2[j] == -INFINITY ? 0.f : exp2f(s2[j] - m_run);
-      ps += p[j];
+      for (int e = 0; e < kHalfKeys; ++e) {
+        const bool ok = tree_unit ? ((my_anc >> (kb + e)) & 1ull) != 0 : kb + e < kend;
+        s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
+      }
     }
-    l_run += ps;
+    float mx[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s2[e], s2[e + 8]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
+    float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    red[hf * kRows + r] = mh;
     // context keys past the cache's end: their V rows are zeroed, so that a
     // non-finite value there cannot reach O through a zero weight
     const int vrows = kend - (key0 + i * kKB);
@@ -357,38 +371,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::fence_proxy_async();
     }
-    // the lead: MMA2_{i-1} complete (P buffer, O and its stage free), then
-    // the block three ahead into that stage
-    if (lead && i >= 1) {
-      if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
-      if (i + kStages - 1 < nb) load_block(i + kStages - 1);
+    __syncthreads();  // ---------------------------------------------- both halves' maxima
+    const float mb = fmaxf(mh, red[(1 - hf) * kRows + r]);
+    float alpha = 1.f;
+    bool need = false;
+    if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
+      alpha = ex2(m_run - mb);
+      need = i > 0;  // O holds earlier blocks (of both halves' keys)
+      l_run *= alpha;
+      m_run = mb;
     }
-    ptx::tc_fence_before();
-    if (__syncthreads_or(need)) {  // some row moved its maximum: rescale O
+    // a row with no valid key yet (padding rows) takes 0 as its reference,
+    // so that masked keys weigh 2^-inf = 0
+    const float mref = m_run == -INFINITY ? 0.f : m_run;
+    float p[kHalfKeys];
+#pragma unroll
+    for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
+    float sm[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm[e] = p[e] + p[e + 8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
+    l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+    // rows whose maximum moved rescale their half of O, once MMA2_{i-1} is done
+    if (__any_sync(0xffffffffu, need)) {
+      if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
       ptx::tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kDh / 32; ++c) {
+      for (int c = 0; c < kHalfCols / 32; ++c) {
+        const uint32_t col = tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c);
         float ov[32];
-        ptx::tmem_ld32(tq + kColO + 32u * c, ov);
+        ptx::tmem_ld32(col, ov);
         ptx::tmem_wait_ld();
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
-        ptx::tmem_st32(tq + kColO + 32u * c, w);
+        ptx::tmem_st32(col, w);
       }
     }
-    // ---- P_i (bf16 hi and lo) -> TMEM, then MMA2 ----
+    // ---- P_i (bf16 hi and lo) -> TMEM ----
     {
-      uint32_t ph[16], pl[16];
+      uint32_t ph[8], pl[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
-      const uint32_t pc = tq + kColP + (uint32_t)(i & 1) * 32;
-      ptx::tmem_st16(pc, ph);
-      ptx::tmem_st16(pc + 16, pl);
+      for (int e = 0; e < 8; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
+      const uint32_t pc = tq + kColP + (uint32_t)(i & 1) * 32 + hf * 8;
+      ptx::tmem_st8(pc, ph);
+      ptx::tmem_st8(pc + 16, pl);
+    }
+    // the lead: MMA2_{i-1} complete (O and its stage free), then the block
+    // three ahead into that stage
+    if (lead && i >= 1) {
+      if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
+      if (i + kStages - 1 < nb) load_block(i + kStages - 1);
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
-    if (__syncthreads_or(bad)) {
+    if (__syncthreads_or(bad)) {  // ------------------------------------ P_i complete
       aborted = true;
       break;
     }
@@ -403,18 +441,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ptx::mbar_wait(&o_bar[(nb - 1) & 1], (uint32_t)(((nb - 1) >> 1) & 1))) bad = true;
   }
   ptx::tc_fence_after();
+  red[hf * kRows + r] = l_run;
+  __syncthreads();
   const bool valid = !aborted && !bad;
   float *pp = A.part + (size_t)blockIdx.x * unit_floats(g);
-  if (real_row) {
+  if (real_row && hf == 0) {
     pp[r] = valid ? m_run : -INFINITY;
-    pp[kRows + r] = valid ? l_run : 0.f;
+    pp[kRows + r] = valid ? red[r] + red[kRows + r] : 0.f;
   }
-  if (valid && nb > 0 && warp * 32 < rows) {
-    float *orow = pp + 2 * kRows + (size_t)r * kDh;
+  if (valid && nb > 0 && quad * 32 < rows) {
+    float *orow = pp + 2 * kRows + (size_t)r * kDh + hf * kHalfCols;
 #pragma unroll 1
-    for (int c = 0; c < kDh / 32; ++c) {
+    for (int c = 0; c < kHalfCols / 32; ++c) {
       float ov[32];
-      ptx::tmem_ld32(tq + kColO + 32u * c, ov);
+      ptx::tmem_ld32(tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c), ov);
       ptx::tmem_wait_ld();
       if (real_row) {
 #pragma unroll
@@ -436,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lead && aborted) {
     for (int j = n_loads - kStages < 0 ? 0 : n_loads - kStages; j < n_loads; ++j)
       (void)ptx::mbar_wait(&kv_bar[j & (kStages - 1)], (uint32_t)((j >> 2) & 1));
-    if (n_mma1 > 0) (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
-    if (n_mma2 > 0) (void)ptx::mbar_wait(&o_bar[(n_mma2 - 1) & 1], (uint32_t)(((n_mma2 - 1) >> 1) & 1));
+    if (n_mma1 > 0)
+      (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
+    if (n_mma2 > 0)
+      (void)ptx::mbar_wait(&o_bar[(n_mma2 - 1) & 1], (uint32_t)(((n_mma2 - 1) >> 1) & 1));
   }
   __syncthreads();
   if (warp == 0) {
@@ -464,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.f / Lsum;
       const int hl = r / N;
       const int hq = kvh * g.G + h0 + hl;
-      float *orow = A.o + (((size_t)lb * N + n_row) * A.Hq + hq) * kDh;
+      float *orow = A.o + (((size_t)lb * N + n_row) * A.Hq + hq) * kDh + hf * kHalfCols;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDh; c0 += 32) {
+      for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
         float acc[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.f;
@@ -475,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float lc = __ldcg(pc + kRows + r);
           if (!(lc > 0.f)) continue;
           const float w = exp2f(__ldcg(pc + r) - M);
-          const float4 *src = reinterpret_cast<const float4 *>(pc + 2 * kRows + (size_t)r * kDh + c0);
+          const float4 *src = reinterpret_cast<const float4 *>(
+              pc + 2 * kRows + (size_t)r * kDh + hf * kHalfCols + c0);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float4 v = __ldcg(src + e);
@@ -582,6 +625,6 @@ extern "C" int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh,
   if (cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemTotal) != cudaSuccess)
     return LBX_ECUDA;
-  tree_attn_kernel<<<(unsigned)A.geo.units, kThreads, kSmemTotal, stream>>>(maps, A);
+  tree_attn_kernel<<<(unsigned)A.geo.units, 2 * kRows, kSmemTotal, stream>>>(maps, A);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
