@@ -87,16 +87,28 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources of kernels that the verify step never launches; a change to them
+# leaves the recorded traffic of the verify workloads valid.
+OTHER_OPS = ("accept_walk.cu", "ddtree_build.cu", "tree_attn.cu")
+
+
+def kernel_source_hash(op: str = "verify") -> str:
+    """Hash of the CUDA sources the op's kernels are built from: every file
+    under csrc/ except the other ops' kernels (verify), or the attention
+    kernel and the PTX wrappers it includes (attn)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tree_verify_linear_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if op == "verify" and name in OTHER_OPS:
+            continue
+        if op == "attn" and name not in ("tree_attn.cu", "tc_ptx.cuh"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, op: str = "verify"):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -105,7 +117,7 @@ def recorded_traffic(workload: str):
     with open(p) as f:
         j = json.load(f)
     e = j.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(op):
         return None
     return int(e["dram_bytes_per_launch"])
 
@@ -694,7 +706,8 @@ def run_attn(args):
                    "T": w.T, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({alg / 1e6:.1f} MB per call)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(w.name, "attn"),
                      "algorithmic_bytes": alg, "kernel": "tree_attn_kernel",
                      "timed": "whole lbx_tree_attention call"},
         "cpu_baseline": cpu,
