@@ -50,34 +50,36 @@ namespace attn {
 
 constexpr int kDh = LBX_ATTN_HEAD_DIM;  // head dimension (256)
 constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
-constexpr int kKB = 32;                 // keys per block
-constexpr int kStages = 4;              // K/V blocks in flight
+constexpr int kKB = 64;                 // keys per block
+constexpr int kKStages = 3;             // K blocks in flight (S runs two blocks ahead)
+constexpr int kVStages = 2;             // V blocks in flight
 constexpr int kMaxNodes = LBX_ATTN_MAX_NODES;
 // Target CTA count the context split aims at (four waves of one CTA per SM
 // on a 152-SM GPU); a function of the shapes only, so that the workspace
 // size does not depend on the device.
 constexpr long long kTargetUnits = 608;
 
-// shared memory: Q tile, K/V stages, ancestor masks, ints, mbarriers
+// shared memory: Q tile, K stages, V stages, ancestor masks, ints, mbarriers
 constexpr int kQBytes = (kDh / 64) * kRows * 128;  // 64 KB, atoms of 64 dh columns
 constexpr int kKVAtom = kKB * 128;                 // one 64-column atom of a block
-constexpr int kKBytes = (kDh / 64) * kKVAtom;      // 16 KB
-constexpr int kStageBytes = 2 * kKBytes;           // K, then V
+constexpr int kKBytes = (kDh / 64) * kKVAtom;      // 32 KB: one K (or V) block
 constexpr int kSmemQ = 0;
-constexpr int kSmemKV = kQBytes;
-constexpr int kSmemAnc = kSmemKV + kStages * kStageBytes;  // uint64 [64]
+constexpr int kSmemK = kQBytes;
+constexpr int kSmemV = kSmemK + kKStages * kKBytes;
+constexpr int kSmemAnc = kSmemV + kVStages * kKBytes;      // uint64 [64]
 constexpr int kSmemRed = kSmemAnc + kMaxNodes * 8;        // float [2][128]
 constexpr int kSmemMisc = kSmemRed + 2 * kRows * 4;       // int [16]
-constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [8]
-constexpr int kSmemTotal = kSmemBars + 8 * 8;
+constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [9]
+constexpr int kSmemTotal = kSmemBars + 9 * 8;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory");
-static_assert(kSmemKV % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled operands");
+static_assert(kSmemK % 1024 == 0 && kSmemV % 1024 == 0 && kKBytes % 1024 == 0,
+              "swizzled operands");
 // tensor memory columns
-constexpr uint32_t kColS = 0;    // S: two 32-column buffers
-constexpr uint32_t kColP = 64;   // P: two buffers of 32 columns (16 hi, 16 lo)
+constexpr uint32_t kColS = 0;    // S: two 64-column buffers
+constexpr uint32_t kColP = 128;  // P: two buffers of 64 columns (32 hi, 32 lo)
 constexpr uint32_t kColO = 256;  // O: 256 columns
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColO + kDh <= kTmemCols && kColP + 64 <= kColO, "tensor memory");
+static_assert(kColO + kDh <= kTmemCols && kColP + 2 * kKB <= kColO, "tensor memory");
 
 // Partition of the work (host and device compute the same).
 struct Geo {
@@ -132,7 +134,7 @@ struct Args {
 };
 
 struct Maps {
-  CUtensorMap kc, vc;  // caches as (dh, Hkv, L*Bq*T), box (64, 1, 32), 128-byte swizzle
+  CUtensorMap kc, vc;  // caches as (dh, Hkv, L*Bq*T), box (64, 1, 64), 128-byte swizzle
   CUtensorMap kt, vt;  // tree keys / values as (dh, Hkv, L*Bq*N)
 };
 
@@ -151,8 +153,8 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Two threads per row: thread (row r, half hf) handles keys 16 hf .. 16 hf +
-// 15 of every block and columns 128 hf .. 128 hf + 127 of O.  Warps w and w+4
+// Two threads per row: thread (row r, half hf) handles keys 32 hf .. 32 hf +
+// 31 of every block and columns 128 hf .. 128 hf + 127 of O.  Warps w and w+4
 // share TMEM lane quadrant w & 3.
 constexpr int kHalfKeys = kKB / 2;
 constexpr int kHalfCols = kDh / 2;
@@ -166,9 +168,10 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   int *misc = reinterpret_cast<int *>(smem + kSmemMisc);  // [0] TMEM base, [1] last CTA
   uint64_t *anc = reinterpret_cast<uint64_t *>(smem + kSmemAnc);
   float *red = reinterpret_cast<float *>(smem + kSmemRed);  // [2][kRows] per-half values
-  uint64_t *kv_bar = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [4]
-  uint64_t *s_bar = kv_bar + 4;                                        // [2]
-  uint64_t *o_bar = kv_bar + 6;                                        // [2]
+  uint64_t *k_bar = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [3]
+  uint64_t *v_bar = k_bar + 3;                                        // [2]
+  uint64_t *s_bar = k_bar + 5;                                        // [2]
+  uint64_t *o_bar = k_bar + 7;                                        // [2]
 
   // ---- the unit: (l*Bq + b, KV head, chunk, tile), tile fastest ----
   long long u = blockIdx.x;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
 
   // ---- set-up ----
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) ptx::mbar_init(kv_bar + i, 1);
+    for (int i = 0; i < 9; ++i) ptx::mbar_init(k_bar + i, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -261,31 +264,37 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   const uint64_t my_anc = tree_unit && real_row ? anc[n_row] : 0ull;
 
   const bool lead = tid == 0;
-  int n_loads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the lead
-  auto load_block = [&](int j) {
-    const int s = j & (kStages - 1);
-    unsigned char *kd = smem + kSmemKV + s * kStageBytes;
-    unsigned char *vd = kd + kKBytes;
-    ptx::mbar_arrive_expect_tx(&kv_bar[s], (uint32_t)kStageBytes);
-    const int z = tree_unit ? lb * N + j * kKB : lb * A.T + key0 + j * kKB;
-    const CUtensorMap *mk = tree_unit ? &maps.kt : &maps.kc;
-    const CUtensorMap *mv = tree_unit ? &maps.vt : &maps.vc;
+  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the lead
+  const int zbase = tree_unit ? lb * N : lb * A.T + key0;  // position row of block 0
+  const CUtensorMap *mk = tree_unit ? &maps.kt : &maps.kc;
+  const CUtensorMap *mv = tree_unit ? &maps.vt : &maps.vc;
+  auto load_k = [&](int j) {
+    const int s = j % kKStages;
+    unsigned char *kd = smem + kSmemK + s * kKBytes;
+    ptx::mbar_arrive_expect_tx(&k_bar[s], (uint32_t)kKBytes);
 #pragma unroll
-    for (int a = 0; a < kDh / 64; ++a) {
-      ptx::tma_load_3d(kd + a * kKVAtom, mk, a * 64, kvh, z, &kv_bar[s]);
-      ptx::tma_load_3d(vd + a * kKVAtom, mv, a * 64, kvh, z, &kv_bar[s]);
-    }
-    ++n_loads;
+    for (int a = 0; a < kDh / 64; ++a)
+      ptx::tma_load_3d(kd + a * kKVAtom, mk, a * 64, kvh, zbase + j * kKB, &k_bar[s]);
+    ++n_kloads;
+  };
+  auto load_v = [&](int j) {
+    const int s = j % kVStages;
+    unsigned char *vd = smem + kSmemV + s * kKBytes;
+    ptx::mbar_arrive_expect_tx(&v_bar[s], (uint32_t)kKBytes);
+#pragma unroll
+    for (int a = 0; a < kDh / 64; ++a)
+      ptx::tma_load_3d(vd + a * kKVAtom, mv, a * 64, kvh, zbase + j * kKB, &v_bar[s]);
+    ++n_vloads;
   };
   // descriptors of the Q tile and of stage 0; the others are fixed offsets
   // (added to the 16-byte address field)
   const uint64_t qdesc = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemQ));
-  const uint64_t kdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemKV));
+  const uint64_t kdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemK));
   const uint64_t vdesc0 =
-      ptx::sdesc(ptx::smem_u32(smem + kSmemKV + kKBytes), (uint32_t)kKVAtom, 1024u, 2u);
-  // S[j & 1] = Q K_j^T: M = 128, N = 32 keys, K = 256 (16 steps)
+      ptx::sdesc(ptx::smem_u32(smem + kSmemV), (uint32_t)kKVAtom, 1024u, 2u);
+  // S[j & 1] = Q K_j^T: M = 128, N = 64 keys, K = 256 (16 steps)
   auto mma1 = [&](int j) {
-    const uint64_t kd = kdesc0 + (uint64_t)(((j & (kStages - 1)) * kStageBytes) >> 4);
+    const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kKBytes) >> 4);
     constexpr uint32_t idesc = ptx::idesc_bf16(128, kKB);
     const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKB;
 #pragma unroll
@@ -300,16 +309,16 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   // O += P_j V_j: A = P (TMEM, hi then lo), B = the V block read MN-major
   // (dh contiguous in 64-column atoms kKVAtom apart, 8-key groups 1024 apart)
   auto mma2 = [&](int j, bool acc) {
-    const uint64_t vd = vdesc0 + (uint64_t)(((j & (kStages - 1)) * kStageBytes) >> 4);
+    const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kKBytes) >> 4);
     constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kDh);
-    const uint32_t pc = tmem + kColP + (uint32_t)(j & 1) * 32;
+    const uint32_t pc = tmem + kColP + (uint32_t)(j & 1) * kKB;
     uint32_t accum = acc ? 1u : 0u;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
       for (int ks = 0; ks < kKB / 16; ++ks) {
-        ptx::mma_bf16_ts(tmem + kColO, pc + pass * 16 + ks * 8, vd + (uint64_t)(ks * 2048 >> 4),
-                         idesc, accum);
+        ptx::mma_bf16_ts(tmem + kColO, pc + pass * (kKB / 2) + ks * 8,
+                         vd + (uint64_t)(ks * 2048 >> 4), idesc, accum);
         accum = 1u;
       }
     ptx::mma_commit(&o_bar[j & 1]);
@@ -318,8 +327,9 @@ __global__ void __launch_bounds__(2 * kRows, 1)
 
   bool bad = false, aborted = false;
   if (lead && nb > 0) {
-    for (int j = 0; j < nb && j < kStages; ++j) load_block(j);
-    if (!ptx::mbar_wait(&kv_bar[0], 0u)) bad = true;
+    for (int j = 0; j < nb && j < kKStages; ++j) load_k(j);
+    for (int j = 0; j < nb && j < kVStages; ++j) load_v(j);
+    if (!ptx::mbar_wait(&k_bar[0], 0u)) bad = true;
     mma1(0);
   }
 
@@ -329,13 +339,17 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     if (!ptx::mbar_wait(&s_bar[i & 1], (uint32_t)((i >> 1) & 1))) bad = true;
     ptx::tc_fence_after();
     float sv[kHalfKeys];
-    ptx::tmem_ld16(tq + kColS + (uint32_t)(i & 1) * kKB + hf * kHalfKeys, sv);
+    ptx::tmem_ld32(tq + kColS + (uint32_t)(i & 1) * kKB + hf * kHalfKeys, sv);
     ptx::tmem_wait_ld();
-    // the next block's scores, into the other buffer (read in iteration i-1)
-    if (lead && i + 1 < nb) {
-      if (!ptx::mbar_wait(&kv_bar[(i + 1) & (kStages - 1)], (uint32_t)(((i + 1) >> 2) & 1)))
-        bad = true;
-      mma1(i + 1);
+    if (lead) {
+      // K_i has been read (S_i is complete): its stage takes block i + 3
+      if (i + kKStages < nb) load_k(i + kKStages);
+      // the next block's scores, into the other buffer (read in iteration i-1)
+      if (i + 1 < nb) {
+        if (!ptx::mbar_wait(&k_bar[(i + 1) % kKStages], (uint32_t)(((i + 1) / kKStages) & 1)))
+          bad = true;
+        mma1(i + 1);
+      }
     }
     // ---- masked, scaled scores and the block maximum of the row ----
     const int kb = key0 + i * kKB + hf * kHalfKeys;  // this half's first key
@@ -350,9 +364,11 @@ __global__ void __launch_bounds__(2 * kRows, 1)
         s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
       }
     }
-    float mx[8];
+    float mx[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s2[e], s2[e + 8]);
+    for (int e = 0; e < 16; ++e) mx[e] = fmaxf(s2[e], s2[e + 16]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
     float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -361,8 +377,8 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     // non-finite value there cannot reach O through a zero weight
     const int vrows = kend - (key0 + i * kKB);
     if (!tree_unit && vrows < kKB && warp == 1) {
-      if (!ptx::mbar_wait(&kv_bar[i & (kStages - 1)], (uint32_t)((i >> 2) & 1))) bad = true;
-      unsigned char *vd = smem + kSmemKV + (i & (kStages - 1)) * kStageBytes + kKBytes;
+      if (!ptx::mbar_wait(&v_bar[i % kVStages], (uint32_t)((i / kVStages) & 1))) bad = true;
+      unsigned char *vd = smem + kSmemV + (i % kVStages) * kKBytes;
       const int zr = kKB - vrows;  // rows to clear, in each of the 4 atoms
       for (int idx = lane; idx < (kDh / 64) * zr * 8; idx += 32) {
         const int a = idx / (zr * 8), rem = idx - a * zr * 8;
@@ -387,9 +403,11 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     float p[kHalfKeys];
 #pragma unroll
     for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
-    float sm[8];
+    float sm[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sm[e] = p[e] + p[e + 8];
+    for (int e = 0; e < 16; ++e) sm[e] = p[e] + p[e + 16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm[e] += sm[e + 8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
     l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
@@ -411,18 +429,18 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     }
     // ---- P_i (bf16 hi and lo) -> TMEM ----
     {
-      uint32_t ph[8], pl[8];
+      uint32_t ph[16], pl[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
-      const uint32_t pc = tq + kColP + (uint32_t)(i & 1) * 32 + hf * 8;
-      ptx::tmem_st8(pc, ph);
-      ptx::tmem_st8(pc + 16, pl);
+      for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
+      const uint32_t pc = tq + kColP + (uint32_t)(i & 1) * kKB + hf * 16;
+      ptx::tmem_st16(pc, ph);
+      ptx::tmem_st16(pc + kKB / 2, pl);
     }
-    // the lead: MMA2_{i-1} complete (O and its stage free), then the block
-    // three ahead into that stage
+    // the lead: MMA2_{i-1} complete (O, its P buffer and its V stage free),
+    // then block i + 1's values into that stage
     if (lead && i >= 1) {
       if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
-      if (i + kStages - 1 < nb) load_block(i + kStages - 1);
+      if (i + 1 < nb) load_v(i + 1);
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
@@ -431,6 +449,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       break;
     }
     if (lead) {
+      if (!ptx::mbar_wait(&v_bar[i % kVStages], (uint32_t)((i / kVStages) & 1))) bad = true;
       ptx::tc_fence_after();
       mma2(i, i > 0);
     }
@@ -474,8 +493,10 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   }
   // drain: copies and MMAs still in flight after an abort
   if (lead && aborted) {
-    for (int j = n_loads - kStages < 0 ? 0 : n_loads - kStages; j < n_loads; ++j)
-      (void)ptx::mbar_wait(&kv_bar[j & (kStages - 1)], (uint32_t)((j >> 2) & 1));
+    for (int j = n_kloads - kKStages < 0 ? 0 : n_kloads - kKStages; j < n_kloads; ++j)
+      (void)ptx::mbar_wait(&k_bar[j % kKStages], (uint32_t)((j / kKStages) & 1));
+    for (int j = n_vloads - kVStages < 0 ? 0 : n_vloads - kVStages; j < n_vloads; ++j)
+      (void)ptx::mbar_wait(&v_bar[j % kVStages], (uint32_t)((j / kVStages) & 1));
     if (n_mma1 > 0)
       (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
     if (n_mma2 > 0)
