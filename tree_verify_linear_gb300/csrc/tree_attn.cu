@@ -13,14 +13,17 @@
 //   online softmax over the key blocks, row by row         -- one thread per row
 //   O += P V                                               -- tensor cores
 //
-// A CTA owns one (layer, request, KV head, row tile, key chunk): row tiles
-// hold at most 128 rows (hp heads x N nodes; G x N = 132 at budget 22 with
-// 6 heads per KV head gives two tiles of 66), key chunks split the context so
-// that the grid fills the GPU, and one extra chunk per row tile holds the
-// tree's own keys, with the ancestor mask.  The two row tiles of a chunk are
-// adjacent CTAs, so the second read of a K/V block is mostly an L2 hit.
-// Each CTA writes its unnormalised partial (running max m, sum l, O) to the
-// workspace; the last CTA of a row tile to finish merges the chunks.
+// The work is the list of (row tile, key block) pairs: per (layer, request,
+// KV head, row tile) the request's context blocks of 64 keys, then one block
+// with the tree's own keys under the ancestor mask.  Row tiles hold at most
+// 128 rows (hp heads x N nodes; 6 x 22 = 132 at budget 22 gives two tiles of
+// 66).  A persistent grid (one CTA per SM) splits the list into equal
+// contiguous ranges, counted from the actual context lengths, so the grid
+// ends together whatever the context lengths; a range covers a few row
+// tiles, and a row tile is covered by one, two or three CTAs.  Each CTA
+// writes the unnormalised partial (running max m, sum l, O) of every row
+// tile it covers to the workspace; the last of a row tile's CTAs to finish
+// merges its partials.
 //
 // Per CTA: the Q tile (128 x 256 bf16, 128-byte swizzled, K-major) stays in
 // shared memory; K and V blocks of 32 keys arrive by TMA, four blocks in
@@ -54,10 +57,10 @@ constexpr int kKB = 64;                 // keys per block
 constexpr int kKStages = 3;             // K blocks in flight (S runs two blocks ahead)
 constexpr int kVStages = 2;             // V blocks in flight
 constexpr int kMaxNodes = LBX_ATTN_MAX_NODES;
-// Target CTA count the context split aims at (four waves of one CTA per SM
-// on a 152-SM GPU); a function of the shapes only, so that the workspace
-// size does not depend on the device.
-constexpr long long kTargetUnits = 608;
+// Largest persistent grid (one CTA per SM; a GPU with more SMs uses this
+// many); the workspace holds one partial per (CTA, row tile) piece, at most
+// kMaxCtas + row tiles of them.
+constexpr int kMaxCtas = 160;
 
 // shared memory: Q tile, K stages, V stages, ancestor masks, ints, mbarriers
 constexpr int kQBytes = (kDh / 64) * kRows * 128;  // 64 KB, atoms of 64 dh columns
@@ -81,19 +84,16 @@ constexpr uint32_t kColO = 256;  // O: 256 columns
 constexpr uint32_t kTmemCols = 512;
 static_assert(kColO + kDh <= kTmemCols && kColP + 2 * kKB <= kColO, "tensor memory");
 
-// Partition of the work (host and device compute the same).
+// Row tiles (host and device compute the same).
 struct Geo {
   int G;         // query heads per KV head
   int tiles;     // row tiles per (layer, request, KV head)
   int hp;        // heads per row tile (the last may hold fewer)
-  int n_chunks;  // context chunks (the tree chunk comes after them)
-  int kc;        // keys per context chunk (a multiple of kKB)
   long long gt;  // (layer, request, KV head, tile) groups
-  long long units;
   int rows_cap;  // hp * N
 };
 
-__host__ __device__ inline Geo geometry(int L, int Bq, int N, int Hq, int Hkv, int T) {
+__host__ __device__ inline Geo geometry(int L, int Bq, int N, int Hq, int Hkv) {
   Geo g;
   g.G = Hq / Hkv;
   g.tiles = 1;
@@ -101,24 +101,16 @@ __host__ __device__ inline Geo geometry(int L, int Bq, int N, int Hq, int Hkv, i
   g.hp = (g.G + g.tiles - 1) / g.tiles;
   g.tiles = (g.G + g.hp - 1) / g.hp;
   g.gt = (long long)L * Bq * Hkv * g.tiles;
-  const int max_blocks = (T + kKB - 1) / kKB;
-  long long nc = (kTargetUnits + g.gt - 1) / g.gt - 1;
-  if (nc > max_blocks) nc = max_blocks;
-  if (nc < 1) nc = 1;
-  const int per = (int)((max_blocks + nc - 1) / nc);
-  g.kc = (per < 1 ? 1 : per) * kKB;
-  g.n_chunks = T > 0 ? (T + g.kc - 1) / g.kc : 0;
-  g.units = g.gt * (g.n_chunks + 1);
   g.rows_cap = g.hp * N;
   return g;
 }
 
-// Floats of one unit's partial: m[128], l[128], then O rows of 256.
+// Floats of one partial: m[128], l[128], then O rows of 256.
 __host__ __device__ inline size_t unit_floats(const Geo &g) {
   return 2 * (size_t)kRows + (size_t)g.rows_cap * kDh;
 }
 __host__ __device__ inline size_t part_bytes(const Geo &g) {
-  return ((size_t)g.units * unit_floats(g) * 4 + 255) & ~(size_t)255;
+  return (((size_t)g.gt + kMaxCtas) * unit_floats(g) * 4 + 255) & ~(size_t)255;
 }
 
 struct Args {
@@ -159,12 +151,17 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr int kHalfKeys = kKB / 2;
 constexpr int kHalfCols = kDh / 2;
 
+// Blocks of request b's row tiles: its context blocks and the tree block.
+__device__ __forceinline__ int blocks_of(const int32_t *ctx_len, int b) {
+  return (ctx_len[b] + kKB - 1) / kKB + 1;
+}
+
 __global__ void __launch_bounds__(2 * kRows, 1)
     tree_attn_kernel(const __grid_constant__ Maps maps, const Args A) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Geo &g = A.geo;
-  const int N = A.N;
+  const int N = A.N, Bq = A.Bq, Hkv = A.Hkv, tiles = g.tiles;
   int *misc = reinterpret_cast<int *>(smem + kSmemMisc);  // [0] TMEM base, [1] last CTA
   uint64_t *anc = reinterpret_cast<uint64_t *>(smem + kSmemAnc);
   float *red = reinterpret_cast<float *>(smem + kSmemRed);  // [2][kRows] per-half values
@@ -173,47 +170,31 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   uint64_t *s_bar = k_bar + 5;                                        // [2]
   uint64_t *o_bar = k_bar + 7;                                        // [2]
 
-  // ---- the unit: (l*Bq + b, KV head, chunk, tile), tile fastest ----
-  long long u = blockIdx.x;
-  const int tile = (int)(u % g.tiles);
-  u /= g.tiles;
-  const int chunk = (int)(u % (g.n_chunks + 1));
-  u /= g.n_chunks + 1;
-  const int kvh = (int)(u % A.Hkv);
-  const int lb = (int)(u / A.Hkv);
-  const int b = lb % A.Bq;
-  const long long gidx = (long long)lb * A.Hkv * g.tiles + (long long)kvh * g.tiles + tile;
-  const bool tree_unit = chunk == g.n_chunks;
-  const int h0 = tile * g.hp;
-  const int hp_t = g.G - h0 < g.hp ? g.G - h0 : g.hp;
-  const int rows = hp_t * N;
-
   // ---- whole-batch validation (the same verdict in every CTA) ----
   {
     int bad_in = 0;
-    for (int i = tid; i < A.Bq * N; i += 2 * kRows) {
+    for (int i = tid; i < Bq * N; i += 2 * kRows) {
       const int n = i % N, p = A.parent[i];
       if (n == 0 ? p != -1 : (p < 0 || p >= n)) bad_in = 1;
     }
-    for (int i = tid; i < A.Bq; i += 2 * kRows)
+    for (int i = tid; i < Bq; i += 2 * kRows)
       if (A.ctx_len[i] < 0 || A.ctx_len[i] > A.T) bad_in = 1;
     if (__syncthreads_or(bad_in)) {
       if (tid == 0 && A.status) *A.status = LBX_ETREE;
       return;
     }
   }
-  const int ctx = A.ctx_len[b];
-  // blocks of this unit, first key, end of the existing keys
-  int nb, key0, kend;
-  if (tree_unit) {
-    nb = (N + kKB - 1) / kKB;
-    key0 = 0;
-    kend = N;
-  } else {
-    key0 = chunk * g.kc;
-    kend = ctx < key0 + g.kc ? ctx : key0 + g.kc;
-    nb = kend > key0 ? (kend - key0 + kKB - 1) / kKB : 0;
-  }
+
+  // ---- the flattened work list and this CTA's range of it ----
+  long long s_all = 0;  // blocks of one (layer, KV head, tile) across the requests
+  for (int b = 0; b < Bq; ++b) s_all += blocks_of(A.ctx_len, b);
+  const long long per_l = (long long)Hkv * tiles * s_all;
+  const long long total = (long long)A.L * per_l;
+  // at most one CTA per block, so that every CTA's range is non-empty
+  const long long P = (long long)gridDim.x < total ? (long long)gridDim.x : total;
+  if ((long long)blockIdx.x >= P) return;
+  const long long x_begin = total * blockIdx.x / P, x_end = total * (blockIdx.x + 1) / P;
+  auto owner = [&](long long x) { return ((x + 1) * P - 1) / total; };
 
   // ---- set-up ----
   if (tid == 0) {
@@ -225,273 +206,378 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
   }
-  if (tree_unit && tid < N) {  // ancestor-or-self mask of node tid
-    uint64_t m = 0;
-    int j = tid;
-    for (int s = 0; s < kMaxNodes && j >= 0; ++s) {
-      m |= 1ull << j;
-      j = A.parent[(size_t)b * N + j];
-    }
-    anc[tid] = m;
-  }
-  // Q tile: row r = hl * N + n (head hl of the tile, node n), zero padding rows
-  {
-    const uint4 *qg = reinterpret_cast<const uint4 *>(A.q);
-    for (int idx = tid; idx < kRows * (kDh / 8); idx += 2 * kRows) {
-      const int r = idx / (kDh / 8), c16 = idx % (kDh / 8);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < rows) {
-        const int hl = r / N, n = r - hl * N;
-        const int hq = kvh * g.G + h0 + hl;
-        v = qg[(((size_t)lb * N + n) * A.Hq + hq) * (kDh / 8) + c16];
-      }
-      const int atom = c16 >> 3, ch = c16 & 7;
-      *reinterpret_cast<uint4 *>(smem + kSmemQ + atom * (kRows * 128) + r * 128 +
-                                 ((ch ^ (r & 7)) << 4)) = v;
-    }
-  }
-  ptx::fence_proxy_async();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int quad = warp & 3, hf = warp >> 2;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quadrant
-
   const int r = quad * 32 + lane;
-  const bool real_row = r < rows;
-  const int n_row = real_row ? r - (r / N) * N : 0;
-  // tree unit: the ancestor bits of this thread's 16 keys of each block
-  const uint64_t my_anc = tree_unit && real_row ? anc[n_row] : 0ull;
-
   const bool lead = tid == 0;
-  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the lead
-  const int zbase = tree_unit ? lb * N : lb * A.T + key0;  // position row of block 0
-  const CUtensorMap *mk = tree_unit ? &maps.kt : &maps.kc;
-  const CUtensorMap *mv = tree_unit ? &maps.vt : &maps.vc;
-  auto load_k = [&](int j) {
-    const int s = j % kKStages;
-    unsigned char *kd = smem + kSmemK + s * kKBytes;
-    ptx::mbar_arrive_expect_tx(&k_bar[s], (uint32_t)kKBytes);
-#pragma unroll
-    for (int a = 0; a < kDh / 64; ++a)
-      ptx::tma_load_3d(kd + a * kKVAtom, mk, a * 64, kvh, zbase + j * kKB, &k_bar[s]);
-    ++n_kloads;
-  };
-  auto load_v = [&](int j) {
-    const int s = j % kVStages;
-    unsigned char *vd = smem + kSmemV + s * kKBytes;
-    ptx::mbar_arrive_expect_tx(&v_bar[s], (uint32_t)kKBytes);
-#pragma unroll
-    for (int a = 0; a < kDh / 64; ++a)
-      ptx::tma_load_3d(vd + a * kKVAtom, mv, a * 64, kvh, zbase + j * kKB, &v_bar[s]);
-    ++n_vloads;
-  };
+
   // descriptors of the Q tile and of stage 0; the others are fixed offsets
   // (added to the 16-byte address field)
   const uint64_t qdesc = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemQ));
   const uint64_t kdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemK));
   const uint64_t vdesc0 =
       ptx::sdesc(ptx::smem_u32(smem + kSmemV), (uint32_t)kKVAtom, 1024u, 2u);
-  // S[j & 1] = Q K_j^T: M = 128, N = 64 keys, K = 256 (16 steps)
-  auto mma1 = [&](int j) {
-    const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kKBytes) >> 4);
-    constexpr uint32_t idesc = ptx::idesc_bf16(128, kKB);
-    const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKB;
-#pragma unroll
-    for (int ks = 0; ks < kDh / 16; ++ks) {
-      const uint64_t ao = (uint64_t)(((ks >> 2) * (kRows * 128) + (ks & 3) * 32) >> 4);
-      const uint64_t bo = (uint64_t)(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
-      ptx::mma_bf16_ss(d, qdesc + ao, kd + bo, idesc, ks > 0 ? 1u : 0u);
-    }
-    ptx::mma_commit(&s_bar[j & 1]);
-    ++n_mma1;
-  };
-  // O += P_j V_j: A = P (TMEM, hi then lo), B = the V block read MN-major
-  // (dh contiguous in 64-column atoms kKVAtom apart, 8-key groups 1024 apart)
-  auto mma2 = [&](int j, bool acc) {
-    const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kKBytes) >> 4);
-    constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kDh);
-    const uint32_t pc = tmem + kColP + (uint32_t)(j & 1) * kKB;
-    uint32_t accum = acc ? 1u : 0u;
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-      for (int ks = 0; ks < kKB / 16; ++ks) {
-        ptx::mma_bf16_ts(tmem + kColO, pc + pass * (kKB / 2) + ks * 8,
-                         vd + (uint64_t)(ks * 2048 >> 4), idesc, accum);
-        accum = 1u;
-      }
-    ptx::mma_commit(&o_bar[j & 1]);
-    ++n_mma2;
-  };
 
+  // Blocks are numbered q = 0, 1, ... across this CTA's segments; stages,
+  // buffers and mbarrier phases follow q.
+  long long q0 = 0;
+  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the lead
   bool bad = false, aborted = false;
-  if (lead && nb > 0) {
-    for (int j = 0; j < nb && j < kKStages; ++j) load_k(j);
-    for (int j = 0; j < nb && j < kVStages; ++j) load_v(j);
-    if (!ptx::mbar_wait(&k_bar[0], 0u)) bad = true;
-    mma1(0);
-  }
 
-  float m_run = -INFINITY, l_run = 0.f;  // base-2 running max; this half's sum
-  for (int i = 0; i < nb; ++i) {
-    // ---- this thread's 16 scores of block i ----
-    if (!ptx::mbar_wait(&s_bar[i & 1], (uint32_t)((i >> 1) & 1))) bad = true;
+  // after an abort a CTA still walks its range, writing empty partials and
+  // counting itself in, so that every group's counter completes and re-arms
+  long long x = x_begin;
+  while (x < x_end) {
+    // ---- locate block x: layer, request, KV head, tile, block of the group ----
+    const int l = (int)(x / per_l);
+    long long rem = x - (long long)l * per_l, base_b = 0;
+    int b = 0, nbr = blocks_of(A.ctx_len, 0);
+    while (rem >= (long long)Hkv * tiles * nbr) {
+      rem -= (long long)Hkv * tiles * nbr;
+      base_b += (long long)Hkv * tiles * nbr;
+      ++b;
+      nbr = blocks_of(A.ctx_len, b);
+    }
+    const int gi = (int)(rem / nbr), blk0 = (int)(rem - (long long)gi * nbr);
+    const int kvh = gi / tiles, tile = gi - kvh * tiles;
+    const int lb = l * Bq + b;
+    const long long gidx = ((long long)lb * Hkv + kvh) * tiles + tile;
+    const long long g_first = (long long)l * per_l + base_b + (long long)gi * nbr;
+    const int blk1 = (int)((x_end - g_first < nbr ? x_end - g_first : nbr));  // end of segment
+    x = g_first + blk1;
+    const int ctx = A.ctx_len[b];
+    const int nctx = nbr - 1;                 // context blocks of the request
+    const int nb = aborted ? 0 : blk1 - blk0;  // blocks of this segment
+    const bool has_tree = blk1 == nbr;        // the segment ends with the tree block
+    const int h0 = tile * g.hp;
+    const int hp_t = g.G - h0 < g.hp ? g.G - h0 : g.hp;
+    const int rows = hp_t * N;
+    const bool real_row = r < rows;
+    const int n_row = real_row ? r - (r / N) * N : 0;
+
+    // ---- Q tile, ancestor masks (all of this segment's earlier MMAs are done) ----
+    if (has_tree && tid < N) {  // ancestor-or-self mask of node tid
+      uint64_t m = 0;
+      int j = tid;
+      for (int s = 0; s < kMaxNodes && j >= 0; ++s) {
+        m |= 1ull << j;
+        j = A.parent[(size_t)b * N + j];
+      }
+      anc[tid] = m;
+    }
+    {
+      const uint4 *qg = reinterpret_cast<const uint4 *>(A.q);
+      for (int idx = tid; idx < kRows * (kDh / 8); idx += 2 * kRows) {
+        const int rr = idx / (kDh / 8), c16 = idx % (kDh / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (rr < rows) {
+          const int hl = rr / N, n = rr - hl * N;
+          const int hq = kvh * g.G + h0 + hl;
+          v = qg[(((size_t)lb * N + n) * A.Hq + hq) * (kDh / 8) + c16];
+        }
+        const int atom = c16 >> 3, ch = c16 & 7;
+        *reinterpret_cast<uint4 *>(smem + kSmemQ + atom * (kRows * 128) + rr * 128 +
+                                   ((ch ^ (rr & 7)) << 4)) = v;
+      }
+    }
+    ptx::fence_proxy_async();
+    ptx::tc_fence_before();
+    __syncthreads();
     ptx::tc_fence_after();
-    float sv[kHalfKeys];
-    ptx::tmem_ld32(tq + kColS + (uint32_t)(i & 1) * kKB + hf * kHalfKeys, sv);
-    ptx::tmem_wait_ld();
-    if (lead) {
-      // K_i has been read (S_i is complete): its stage takes block i + 3
-      if (i + kKStages < nb) load_k(i + kKStages);
-      // the next block's scores, into the other buffer (read in iteration i-1)
-      if (i + 1 < nb) {
-        if (!ptx::mbar_wait(&k_bar[(i + 1) % kKStages], (uint32_t)(((i + 1) / kKStages) & 1)))
-          bad = true;
-        mma1(i + 1);
+    const uint64_t my_anc = has_tree && real_row ? anc[n_row] : 0ull;
+
+    // block i of the segment: context block blk0 + i, or the tree block
+    auto z_of = [&](int i) {
+      const int jb = blk0 + i;
+      return jb < nctx ? lb * A.T + jb * kKB : lb * N;
+    };
+    auto map_k = [&](int i) { return blk0 + i < nctx ? &maps.kc : &maps.kt; };
+    auto map_v = [&](int i) { return blk0 + i < nctx ? &maps.vc : &maps.vt; };
+    auto load_k = [&](int i) {
+      const long long q = q0 + i;
+      const int s = (int)(q % kKStages);
+      unsigned char *kd = smem + kSmemK + s * kKBytes;
+      ptx::mbar_arrive_expect_tx(&k_bar[s], (uint32_t)kKBytes);
+#pragma unroll
+      for (int a = 0; a < kDh / 64; ++a)
+        ptx::tma_load_3d(kd + a * kKVAtom, map_k(i), a * 64, kvh, z_of(i), &k_bar[s]);
+      ++n_kloads;
+    };
+    auto load_v = [&](int i) {
+      const long long q = q0 + i;
+      const int s = (int)(q % kVStages);
+      unsigned char *vd = smem + kSmemV + s * kKBytes;
+      ptx::mbar_arrive_expect_tx(&v_bar[s], (uint32_t)kKBytes);
+#pragma unroll
+      for (int a = 0; a < kDh / 64; ++a)
+        ptx::tma_load_3d(vd + a * kKVAtom, map_v(i), a * 64, kvh, z_of(i), &v_bar[s]);
+      ++n_vloads;
+    };
+    // S[q & 1] = Q K^T of segment block i: M = 128, N = 64 keys, K = 256
+    auto mma1 = [&](int i) {
+      const long long q = q0 + i;
+      const uint64_t kd = kdesc0 + (uint64_t)(((q % kKStages) * kKBytes) >> 4);
+      constexpr uint32_t idesc = ptx::idesc_bf16(128, kKB);
+      const uint32_t d = tmem + kColS + (uint32_t)(q & 1) * kKB;
+#pragma unroll
+      for (int ks = 0; ks < kDh / 16; ++ks) {
+        const uint64_t ao = (uint64_t)(((ks >> 2) * (kRows * 128) + (ks & 3) * 32) >> 4);
+        const uint64_t bo = (uint64_t)(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
+        ptx::mma_bf16_ss(d, qdesc + ao, kd + bo, idesc, ks > 0 ? 1u : 0u);
       }
+      ptx::mma_commit(&s_bar[q & 1]);
+      ++n_mma1;
+    };
+    // O += P V of segment block i: A = P (TMEM, hi then lo), B = the V block
+    // read MN-major (dh contiguous in 64-column atoms, 8-key groups 1024 apart)
+    auto mma2 = [&](int i, bool acc) {
+      const long long q = q0 + i;
+      const uint64_t vd = vdesc0 + (uint64_t)(((q % kVStages) * kKBytes) >> 4);
+      constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kDh);
+      const uint32_t pc = tmem + kColP + (uint32_t)(q & 1) * kKB;
+      uint32_t accum = acc ? 1u : 0u;
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < kKB / 16; ++ks) {
+          ptx::mma_bf16_ts(tmem + kColO, pc + pass * (kKB / 2) + ks * 8,
+                           vd + (uint64_t)(ks * 2048 >> 4), idesc, accum);
+          accum = 1u;
+        }
+      ptx::mma_commit(&o_bar[q & 1]);
+      ++n_mma2;
+    };
+
+    if (lead && nb > 0) {
+      for (int i = 0; i < nb && i < kKStages; ++i) load_k(i);
+      for (int i = 0; i < nb && i < kVStages; ++i) load_v(i);
+      if (!ptx::mbar_wait(&k_bar[q0 % kKStages], (uint32_t)((q0 / kKStages) & 1))) bad = true;
+      mma1(0);
     }
-    // ---- masked, scaled scores and the block maximum of the row ----
-    const int kb = key0 + i * kKB + hf * kHalfKeys;  // this half's first key
-    float s2[kHalfKeys];
-    if (!tree_unit && kb + kHalfKeys <= kend) {
-#pragma unroll
-      for (int e = 0; e < kHalfKeys; ++e) s2[e] = sv[e] * A.scale_log2;
-    } else {
-#pragma unroll
-      for (int e = 0; e < kHalfKeys; ++e) {
-        const bool ok = tree_unit ? ((my_anc >> (kb + e)) & 1ull) != 0 : kb + e < kend;
-        s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
-      }
-    }
-    float mx[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) mx[e] = fmaxf(s2[e], s2[e + 16]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
-    float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    red[hf * kRows + r] = mh;
-    // context keys past the cache's end: their V rows are zeroed, so that a
-    // non-finite value there cannot reach O through a zero weight
-    const int vrows = kend - (key0 + i * kKB);
-    if (!tree_unit && vrows < kKB && warp == 1) {
-      if (!ptx::mbar_wait(&v_bar[i % kVStages], (uint32_t)((i / kVStages) & 1))) bad = true;
-      unsigned char *vd = smem + kSmemV + (i % kVStages) * kKBytes;
-      const int zr = kKB - vrows;  // rows to clear, in each of the 4 atoms
-      for (int idx = lane; idx < (kDh / 64) * zr * 8; idx += 32) {
-        const int a = idx / (zr * 8), rem = idx - a * zr * 8;
-        *reinterpret_cast<uint4 *>(vd + a * kKVAtom + (vrows + rem / 8) * 128 + (rem % 8) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-      ptx::fence_proxy_async();
-    }
-    __syncthreads();  // ---------------------------------------------- both halves' maxima
-    const float mb = fmaxf(mh, red[(1 - hf) * kRows + r]);
-    float alpha = 1.f;
-    bool need = false;
-    if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
-      alpha = ex2(m_run - mb);
-      need = i > 0;  // O holds earlier blocks (of both halves' keys)
-      l_run *= alpha;
-      m_run = mb;
-    }
-    // a row with no valid key yet (padding rows) takes 0 as its reference,
-    // so that masked keys weigh 2^-inf = 0
-    const float mref = m_run == -INFINITY ? 0.f : m_run;
-    float p[kHalfKeys];
-#pragma unroll
-    for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
-    float sm[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) sm[e] = p[e] + p[e + 16];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sm[e] += sm[e + 8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
-    l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
-    // rows whose maximum moved rescale their half of O, once MMA2_{i-1} is done
-    if (__any_sync(0xffffffffu, need)) {
-      if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
+
+    float m_run = -INFINITY, l_run = 0.f;  // base-2 running max; this half's sum
+    for (int i = 0; i < nb; ++i) {
+      const long long q = q0 + i;
+      const bool tree_blk = blk0 + i == nctx;
+      // ---- this thread's 32 scores of the block ----
+      if (!ptx::mbar_wait(&s_bar[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
       ptx::tc_fence_after();
+      float sv[kHalfKeys];
+      ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
+      ptx::tmem_wait_ld();
+      if (lead) {
+        // K of this block has been read (S is complete): its stage takes block i + 3
+        if (i + kKStages < nb) load_k(i + kKStages);
+        // the next block's scores, into the other buffer (read one block ago)
+        if (i + 1 < nb) {
+          if (!ptx::mbar_wait(&k_bar[(q + 1) % kKStages], (uint32_t)(((q + 1) / kKStages) & 1)))
+            bad = true;
+          mma1(i + 1);
+        }
+      }
+      // ---- masked, scaled scores and the block maximum of the row ----
+      const int key0 = tree_blk ? 0 : (blk0 + i) * kKB;  // key (or node) of column 0
+      const int kend = tree_blk ? N : ctx;
+      const int kb = key0 + hf * kHalfKeys;  // this half's first key
+      float s2[kHalfKeys];
+      if (!tree_blk && kb + kHalfKeys <= kend) {
+#pragma unroll
+        for (int e = 0; e < kHalfKeys; ++e) s2[e] = sv[e] * A.scale_log2;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kHalfKeys; ++e) {
+          const bool ok = tree_blk ? ((my_anc >> (kb + e)) & 1ull) != 0 : kb + e < kend;
+          s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
+        }
+      }
+      float mx[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) mx[e] = fmaxf(s2[e], s2[e + 16]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
+      const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      red[hf * kRows + r] = mh;
+      // context keys past the cache's end: their V rows are zeroed, so that a
+      // non-finite value there cannot reach O through a zero weight
+      const int vrows = kend - key0;
+      if (!tree_blk && vrows < kKB && warp == 1) {
+        if (!ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1))) bad = true;
+        unsigned char *vd = smem + kSmemV + (int)(q % kVStages) * kKBytes;
+        const int zr = kKB - vrows;  // rows to clear, in each of the 4 atoms
+        for (int idx = lane; idx < (kDh / 64) * zr * 8; idx += 32) {
+          const int a = idx / (zr * 8), rm = idx - a * zr * 8;
+          *reinterpret_cast<uint4 *>(vd + a * kKVAtom + (vrows + rm / 8) * 128 + (rm % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async();
+      }
+      __syncthreads();  // -------------------------------------------- both halves' maxima
+      const float mb = fmaxf(mh, red[(1 - hf) * kRows + r]);
+      float alpha = 1.f;
+      bool need = false;
+      if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
+        alpha = ex2(m_run - mb);
+        need = i > 0;  // O holds earlier blocks (of both halves' keys)
+        l_run *= alpha;
+        m_run = mb;
+      }
+      // a row with no valid key yet (padding rows) takes 0 as its reference,
+      // so that masked keys weigh 2^-inf = 0
+      const float mref = m_run == -INFINITY ? 0.f : m_run;
+      float p[kHalfKeys];
+#pragma unroll
+      for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
+      float sm[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sm[e] = p[e] + p[e + 16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm[e] += sm[e + 8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
+      l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+      // rows whose maximum moved rescale their half of O, once the previous
+      // P V product is done
+      if (__any_sync(0xffffffffu, need)) {
+        if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kHalfCols / 32; ++c) {
+          const uint32_t col = tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c);
+          float ov[32];
+          ptx::tmem_ld32(col, ov);
+          ptx::tmem_wait_ld();
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
+          ptx::tmem_st32(col, w);
+        }
+      }
+      // ---- P (bf16 hi and lo) -> TMEM ----
+      {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
+        const uint32_t pc = tq + kColP + (uint32_t)(q & 1) * kKB + hf * 16;
+        ptx::tmem_st16(pc, ph);
+        ptx::tmem_st16(pc + kKB / 2, pl);
+      }
+      // the lead: the previous P V product complete (O, its P buffer and its
+      // V stage free), then the next block's values into that stage
+      if (lead && i >= 1) {
+        if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
+        if (i + 1 < nb) load_v(i + 1);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      if (__syncthreads_or(bad)) {  // ---------------------------------- P complete
+        aborted = true;
+        break;
+      }
+      if (lead) {
+        if (!ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1))) bad = true;
+        ptx::tc_fence_after();
+        mma2(i, i > 0);
+      }
+    }
+
+    // ---- this segment's partial -> workspace (slot CTA + group) ----
+    if (!aborted && nb > 0) {
+      const long long ql = q0 + nb - 1;
+      if (!ptx::mbar_wait(&o_bar[ql & 1], (uint32_t)((ql >> 1) & 1))) bad = true;
+    }
+    ptx::tc_fence_after();
+    red[hf * kRows + r] = l_run;
+    __syncthreads();
+    const bool valid = !aborted && !bad;
+    float *pp = A.part + (size_t)(blockIdx.x + gidx) * unit_floats(g);
+    if (real_row && hf == 0) {
+      pp[r] = valid && nb > 0 ? m_run : -INFINITY;
+      pp[kRows + r] = valid && nb > 0 ? red[r] + red[kRows + r] : 0.f;
+    }
+    if (valid && nb > 0 && quad * 32 < rows) {
+      float *orow = pp + 2 * kRows + (size_t)r * kDh + hf * kHalfCols;
 #pragma unroll 1
       for (int c = 0; c < kHalfCols / 32; ++c) {
-        const uint32_t col = tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c);
         float ov[32];
-        ptx::tmem_ld32(col, ov);
+        ptx::tmem_ld32(tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c), ov);
         ptx::tmem_wait_ld();
-        uint32_t w[32];
+        if (real_row) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
-        ptx::tmem_st32(col, w);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(orow + 32 * c + e) =
+                make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+        }
       }
     }
-    // ---- P_i (bf16 hi and lo) -> TMEM ----
-    {
-      uint32_t ph[16], pl[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
-      const uint32_t pc = tq + kColP + (uint32_t)(i & 1) * kKB + hf * 16;
-      ptx::tmem_st16(pc, ph);
-      ptx::tmem_st16(pc + kKB / 2, pl);
-    }
-    // the lead: MMA2_{i-1} complete (O, its P buffer and its V stage free),
-    // then block i + 1's values into that stage
-    if (lead && i >= 1) {
-      if (!ptx::mbar_wait(&o_bar[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) bad = true;
-      if (i + 1 < nb) load_v(i + 1);
-    }
-    ptx::tmem_wait_st();
+    q0 += nb;
+    if (bad && A.status) *A.status = LBX_ETIMEOUT;
+    __threadfence();
     ptx::tc_fence_before();
-    if (__syncthreads_or(bad)) {  // ------------------------------------ P_i complete
-      aborted = true;
-      break;
+    // the group's pieces: the CTAs owning its first and last block
+    const long long c_first = owner(g_first), c_last = owner(g_first + nbr - 1);
+    if (tid == 0) {
+      const unsigned prev = atomicAdd(&A.counters[gidx], 1u);
+      misc[1] = (long long)prev == c_last - c_first ? 1 : 0;
     }
-    if (lead) {
-      if (!ptx::mbar_wait(&v_bar[i % kVStages], (uint32_t)((i / kVStages) & 1))) bad = true;
-      ptx::tc_fence_after();
-      mma2(i, i > 0);
+    __syncthreads();
+    // ---- the last piece of a group merges its partials ----
+    if (misc[1]) {
+      __threadfence();
+      if (real_row) {
+        float M = -INFINITY;
+        for (long long c = c_first; c <= c_last; ++c) {
+          const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+          M = fmaxf(M, __ldcg(pc + r));
+        }
+        float Lsum = 0.f;
+        for (long long c = c_first; c <= c_last; ++c) {
+          const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+          const float lc = __ldcg(pc + kRows + r);
+          if (lc > 0.f) Lsum += exp2f(__ldcg(pc + r) - M) * lc;
+        }
+        const float inv = 1.f / Lsum;
+        const int hl = r / N;
+        const int hq = kvh * g.G + h0 + hl;
+        float *orow = A.o + (((size_t)lb * N + n_row) * A.Hq + hq) * kDh + hf * kHalfCols;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          for (long long c = c_first; c <= c_last; ++c) {
+            const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+            const float lc = __ldcg(pc + kRows + r);
+            if (!(lc > 0.f)) continue;
+            const float w = exp2f(__ldcg(pc + r) - M);
+            const float4 *src = reinterpret_cast<const float4 *>(
+                pc + 2 * kRows + (size_t)r * kDh + hf * kHalfCols + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 v = __ldcg(src + e);
+              acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
+              acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
+              acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
+              acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            __stcs(reinterpret_cast<float4 *>(orow + c0 + e),
+                   make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv,
+                               acc[e + 3] * inv));
+        }
+      }
+      if (tid == 0) A.counters[gidx] = 0u;  // re-armed for the next call
     }
+    __syncthreads();  // red, misc and the Q tile are reused by the next segment
   }
 
-  // ---- partial of this unit -> workspace ----
-  if (!aborted && nb > 0) {
-    if (!ptx::mbar_wait(&o_bar[(nb - 1) & 1], (uint32_t)(((nb - 1) >> 1) & 1))) bad = true;
-  }
-  ptx::tc_fence_after();
-  red[hf * kRows + r] = l_run;
-  __syncthreads();
-  const bool valid = !aborted && !bad;
-  float *pp = A.part + (size_t)blockIdx.x * unit_floats(g);
-  if (real_row && hf == 0) {
-    pp[r] = valid ? m_run : -INFINITY;
-    pp[kRows + r] = valid ? red[r] + red[kRows + r] : 0.f;
-  }
-  if (valid && nb > 0 && quad * 32 < rows) {
-    float *orow = pp + 2 * kRows + (size_t)r * kDh + hf * kHalfCols;
-#pragma unroll 1
-    for (int c = 0; c < kHalfCols / 32; ++c) {
-      float ov[32];
-      ptx::tmem_ld32(tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c), ov);
-      ptx::tmem_wait_ld();
-      if (real_row) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4 *>(orow + 32 * c + e) =
-              make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-      }
-    }
-  }
-  if (bad && A.status) *A.status = LBX_ETIMEOUT;
-  __threadfence();
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(&A.counters[gidx], 1u);
-    misc[1] = prev == (unsigned)g.n_chunks ? 1 : 0;  // n_chunks + 1 units per group
-  }
-  // drain: copies and MMAs still in flight after an abort
+  // ---- drain: copies and MMAs still in flight after an abort ----
   if (lead && aborted) {
     for (int j = n_kloads - kKStages < 0 ? 0 : n_kloads - kKStages; j < n_kloads; ++j)
       (void)ptx::mbar_wait(&k_bar[j % kKStages], (uint32_t)((j / kKStages) & 1));
@@ -502,60 +588,11 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     if (n_mma2 > 0)
       (void)ptx::mbar_wait(&o_bar[(n_mma2 - 1) & 1], (uint32_t)(((n_mma2 - 1) >> 1) & 1));
   }
+  ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
-  }
-
-  // ---- the last unit of a row tile merges the chunks ----
-  if (misc[1]) {
-    __threadfence();
-    if (real_row) {
-      const long long first = (long long)blockIdx.x - (long long)chunk * g.tiles;
-      float M = -INFINITY;
-      for (int c = 0; c <= g.n_chunks; ++c) {
-        const float *pc = A.part + (size_t)(first + (long long)c * g.tiles) * unit_floats(g);
-        M = fmaxf(M, __ldcg(pc + r));
-      }
-      float Lsum = 0.f;
-      for (int c = 0; c <= g.n_chunks; ++c) {
-        const float *pc = A.part + (size_t)(first + (long long)c * g.tiles) * unit_floats(g);
-        const float lc = __ldcg(pc + kRows + r);
-        if (lc > 0.f) Lsum += exp2f(__ldcg(pc + r) - M) * lc;
-      }
-      const float inv = 1.f / Lsum;
-      const int hl = r / N;
-      const int hq = kvh * g.G + h0 + hl;
-      float *orow = A.o + (((size_t)lb * N + n_row) * A.Hq + hq) * kDh + hf * kHalfCols;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
-        float acc[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-        for (int c = 0; c <= g.n_chunks; ++c) {
-          const float *pc = A.part + (size_t)(first + (long long)c * g.tiles) * unit_floats(g);
-          const float lc = __ldcg(pc + kRows + r);
-          if (!(lc > 0.f)) continue;
-          const float w = exp2f(__ldcg(pc + r) - M);
-          const float4 *src = reinterpret_cast<const float4 *>(
-              pc + 2 * kRows + (size_t)r * kDh + hf * kHalfCols + c0);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v = __ldcg(src + e);
-            acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
-            acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
-            acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
-            acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          __stcs(reinterpret_cast<float4 *>(orow + c0 + e),
-                 make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv));
-      }
-    }
-    if (tid == 0) A.counters[gidx] = 0u;  // re-armed for the next call
   }
 }
 
@@ -588,7 +625,8 @@ bool encode_kv(CUtensorMap *map, const void *base, int Hkv, long long rows) {
 }
 
 size_t attn_ws_bytes(int L, int Bq, int N, int Hq, int Hkv, int T) {
-  const Geo g = geometry(L, Bq, N, Hq, Hkv, T);
+  (void)T;
+  const Geo g = geometry(L, Bq, N, Hq, Hkv);
   return part_bytes(g) + (((size_t)g.gt * 4 + 255) & ~(size_t)255);
 }
 
@@ -597,8 +635,8 @@ bool shapes_ok(int L, int Bq, int N, int Hq, int Hkv, int dh, int T) {
   if (dh != kDh || Hq % Hkv != 0) return false;
   if ((long long)L * Bq * T > 0x7fffffffLL || (long long)L * Bq * N * Hq > 0x7fffffffLL)
     return false;
-  const Geo g = geometry(L, Bq, N, Hq, Hkv, T);
-  return g.units <= 0x7fffffffLL;
+  const Geo g = geometry(L, Bq, N, Hq, Hkv);
+  return g.gt <= 0x7fffffffLL;
 }
 
 }  // namespace attn
@@ -636,7 +674,7 @@ extern "C" int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh,
     return LBX_ECUDA;
   Args A;
   A.L = L, A.Bq = Bq, A.N = N, A.Hq = Hq, A.Hkv = Hkv, A.T = T;
-  A.geo = geometry(L, Bq, N, Hq, Hkv, T);
+  A.geo = geometry(L, Bq, N, Hq, Hkv);
   A.scale_log2 = scale * 1.4426950408889634f;
   A.q = q, A.ctx_len = ctx_len, A.parent = parent, A.o = o;
   A.part = static_cast<float *>(workspace);
@@ -646,6 +684,11 @@ extern "C" int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh,
   if (cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemTotal) != cudaSuccess)
     return LBX_ECUDA;
-  tree_attn_kernel<<<(unsigned)A.geo.units, 2 * kRows, kSmemTotal, stream>>>(maps, A);
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
+    return LBX_ECUDA;
+  const int grid = nsm < kMaxCtas ? nsm : kMaxCtas;  // one CTA per SM, persistent
+  tree_attn_kernel<<<(unsigned)grid, 2 * kRows, kSmemTotal, stream>>>(maps, A);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
