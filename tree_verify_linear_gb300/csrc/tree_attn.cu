@@ -17,13 +17,15 @@
 // KV head, row tile) the request's context blocks of 64 keys, then one block
 // with the tree's own keys under the ancestor mask.  Row tiles hold at most
 // 128 rows (hp heads x N nodes; 6 x 22 = 132 at budget 22 gives two tiles of
-// 66).  A persistent grid (one CTA per SM) splits the list into equal
-// contiguous ranges, counted from the actual context lengths, so the grid
-// ends together whatever the context lengths; a range covers a few row
-// tiles, and a row tile is covered by one, two or three CTAs.  Each CTA
-// writes the unnormalised partial (running max m, sum l, O) of every row
-// tile it covers to the workspace; the last of a row tile's CTAs to finish
-// merges its partials.
+// 66).  A persistent grid (one CTA per SM) is cut into groups of `tiles`
+// consecutive CTAs; the groups split the list of (layer, request, KV head,
+// key block) into equal contiguous ranges, counted from the actual context
+// lengths, and the CTAs of a group take one row tile each of the same range,
+// so each K/V block is read from DRAM once and from L2 by the group's other
+// CTAs.  A range covers a few (layer, request, KV head) groups, and a row
+// tile is covered by one, two or three CTAs.  Each CTA writes the
+// unnormalised partial (running max m, sum l, O) of every row tile it covers
+// to the workspace; the last of a row tile's CTAs to finish merges them.
 //
 // Per CTA: the Q tile (128 x 256 bf16, 128-byte swizzled, K-major) stays in
 // shared memory; K and V blocks of 32 keys arrive by TMA, four blocks in
@@ -110,7 +112,7 @@ __host__ __device__ inline size_t unit_floats(const Geo &g) {
   return 2 * (size_t)kRows + (size_t)g.rows_cap * kDh;
 }
 __host__ __device__ inline size_t part_bytes(const Geo &g) {
-  return (((size_t)g.gt + kMaxCtas) * unit_floats(g) * 4 + 255) & ~(size_t)255;
+  return (((size_t)g.gt + kMaxCtas + g.tiles) * unit_floats(g) * 4 + 255) & ~(size_t)255;
 }
 
 struct Args {
@@ -185,15 +187,19 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     }
   }
 
-  // ---- the flattened work list and this CTA's range of it ----
-  long long s_all = 0;  // blocks of one (layer, KV head, tile) across the requests
+  // ---- the flattened work list and this CTA group's range of it ----
+  long long s_all = 0;  // blocks of one (layer, KV head) across the requests
   for (int b = 0; b < Bq; ++b) s_all += blocks_of(A.ctx_len, b);
-  const long long per_l = (long long)Hkv * tiles * s_all;
+  const long long per_l = (long long)Hkv * s_all;
   const long long total = (long long)A.L * per_l;
-  // at most one CTA per block, so that every CTA's range is non-empty
-  const long long P = (long long)gridDim.x < total ? (long long)gridDim.x : total;
-  if ((long long)blockIdx.x >= P) return;
-  const long long x_begin = total * blockIdx.x / P, x_end = total * (blockIdx.x + 1) / P;
+  // groups of `tiles` CTAs, at most one group per block, so that every
+  // group's range is non-empty
+  long long P = (long long)gridDim.x / tiles;
+  if (P > total) P = total;
+  const long long cg = blockIdx.x / tiles;
+  const int tile = (int)(blockIdx.x - cg * tiles);
+  if (cg >= P) return;
+  const long long x_begin = total * cg / P, x_end = total * (cg + 1) / P;
   auto owner = [&](long long x) { return ((x + 1) * P - 1) / total; };
 
   // ---- set-up ----
@@ -235,17 +241,17 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     const int l = (int)(x / per_l);
     long long rem = x - (long long)l * per_l, base_b = 0;
     int b = 0, nbr = blocks_of(A.ctx_len, 0);
-    while (rem >= (long long)Hkv * tiles * nbr) {
-      rem -= (long long)Hkv * tiles * nbr;
-      base_b += (long long)Hkv * tiles * nbr;
+    while (rem >= (long long)Hkv * nbr) {
+      rem -= (long long)Hkv * nbr;
+      base_b += (long long)Hkv * nbr;
       ++b;
       nbr = blocks_of(A.ctx_len, b);
     }
-    const int gi = (int)(rem / nbr), blk0 = (int)(rem - (long long)gi * nbr);
-    const int kvh = gi / tiles, tile = gi - kvh * tiles;
+    const int kvh = (int)(rem / nbr), blk0 = (int)(rem - (long long)kvh * nbr);
     const int lb = l * Bq + b;
-    const long long gidx = ((long long)lb * Hkv + kvh) * tiles + tile;
-    const long long g_first = (long long)l * per_l + base_b + (long long)gi * nbr;
+    const long long kvg = (long long)lb * Hkv + kvh;  // (layer, request, KV head)
+    const long long gidx = kvg * tiles + tile;        // its row tile of this CTA
+    const long long g_first = (long long)l * per_l + base_b + (long long)kvh * nbr;
     const int blk1 = (int)((x_end - g_first < nbr ? x_end - g_first : nbr));  // end of segment
     x = g_first + blk1;
     const int ctx = A.ctx_len[b];
@@ -485,7 +491,8 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       }
     }
 
-    // ---- this segment's partial -> workspace (slot CTA + group) ----
+    // ---- this segment's partial -> workspace (slot (CTA group + KV group)
+    // x tiles + tile, unique since along the list either advances by one) ----
     if (!aborted && nb > 0) {
       const long long ql = q0 + nb - 1;
       if (!ptx::mbar_wait(&o_bar[ql & 1], (uint32_t)((ql >> 1) & 1))) bad = true;
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     red[hf * kRows + r] = l_run;
     __syncthreads();
     const bool valid = !aborted && !bad;
-    float *pp = A.part + (size_t)(blockIdx.x + gidx) * unit_floats(g);
+    float *pp = A.part + (size_t)((cg + kvg) * tiles + tile) * unit_floats(g);
     if (real_row && hf == 0) {
       pp[r] = valid && nb > 0 ? m_run : -INFINITY;
       pp[kRows + r] = valid && nb > 0 ? red[r] + red[kRows + r] : 0.f;
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     if (bad && A.status) *A.status = LBX_ETIMEOUT;
     __threadfence();
     ptx::tc_fence_before();
-    // the group's pieces: the CTAs owning its first and last block
+    // the row tile's pieces: the CTA groups owning its first and last block
     const long long c_first = owner(g_first), c_last = owner(g_first + nbr - 1);
     if (tid == 0) {
       const unsigned prev = atomicAdd(&A.counters[gidx], 1u);
@@ -531,12 +538,12 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       if (real_row) {
         float M = -INFINITY;
         for (long long c = c_first; c <= c_last; ++c) {
-          const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+          const float *pc = A.part + (size_t)((c + kvg) * tiles + tile) * unit_floats(g);
           M = fmaxf(M, __ldcg(pc + r));
         }
         float Lsum = 0.f;
         for (long long c = c_first; c <= c_last; ++c) {
-          const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+          const float *pc = A.part + (size_t)((c + kvg) * tiles + tile) * unit_floats(g);
           const float lc = __ldcg(pc + kRows + r);
           if (lc > 0.f) Lsum += exp2f(__ldcg(pc + r) - M) * lc;
         }
@@ -550,7 +557,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = 0.f;
           for (long long c = c_first; c <= c_last; ++c) {
-            const float *pc = A.part + (size_t)(c + gidx) * unit_floats(g);
+            const float *pc = A.part + (size_t)((c + kvg) * tiles + tile) * unit_floats(g);
             const float lc = __ldcg(pc + kRows + r);
             if (!(lc > 0.f)) continue;
             const float w = exp2f(__ldcg(pc + r) - M);
@@ -688,7 +695,10 @@ extern "C" int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
     return LBX_ECUDA;
-  const int grid = nsm < kMaxCtas ? nsm : kMaxCtas;  // one CTA per SM, persistent
+  // one CTA per SM, persistent, in groups of `tiles` (at least one group)
+  int grid = nsm < kMaxCtas ? nsm : kMaxCtas;
+  grid = grid / A.geo.tiles * A.geo.tiles;
+  if (grid < A.geo.tiles) grid = A.geo.tiles;
   tree_attn_kernel<<<(unsigned)grid, 2 * kRows, kSmemTotal, stream>>>(maps, A);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
