@@ -218,7 +218,11 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   const int quad = warp & 3, hf = warp >> 2;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quadrant
   const int r = quad * 32 + lane;
-  const bool lead = tid == 0;
+  // two issuing threads in different warps: lead_s (warp 4) the S = Q K^T
+  // products and the K copies, lead (warp 0) the O += P V products and the
+  // V copies; each commit tracks its own thread's MMAs, and the two streams
+  // share no tensor memory
+  const bool lead = tid == 0, lead_s = tid == kRows;
 
   // descriptors of the Q tile and of stage 0; the others are fixed offsets
   // (added to the 16-byte address field)
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   // Blocks are numbered q = 0, 1, ... across this CTA's segments; stages,
   // buffers and mbarrier phases follow q.
   long long q0 = 0;
-  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the lead
+  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by lead_s / lead
   bool bad = false, aborted = false;
 
   // after an abort a CTA still walks its range, writing empty partials and
@@ -357,12 +361,13 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       ++n_mma2;
     };
 
-    if (lead && nb > 0) {
+    if (lead_s && nb > 0) {
       for (int i = 0; i < nb && i < kKStages; ++i) load_k(i);
-      for (int i = 0; i < nb && i < kVStages; ++i) load_v(i);
       if (!ptx::mbar_wait(&k_bar[q0 % kKStages], (uint32_t)((q0 / kKStages) & 1))) bad = true;
       mma1(0);
     }
+    if (lead && nb > 0)
+      for (int i = 0; i < nb && i < kVStages; ++i) load_v(i);
 
     float m_run = -INFINITY, l_run = 0.f;  // base-2 running max; this half's sum
     for (int i = 0; i < nb; ++i) {
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       float sv[kHalfKeys];
       ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
       ptx::tmem_wait_ld();
-      if (lead) {
+      if (lead_s) {
         // K of this block has been read (S is complete): its stage takes block i + 3
         if (i + kKStages < nb) load_k(i + kKStages);
         // the next block's scores, into the other buffer (read one block ago)
@@ -585,13 +590,15 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   }
 
   // ---- drain: copies and MMAs still in flight after an abort ----
-  if (lead && aborted) {
+  if (lead_s && aborted) {
     for (int j = n_kloads - kKStages < 0 ? 0 : n_kloads - kKStages; j < n_kloads; ++j)
       (void)ptx::mbar_wait(&k_bar[j % kKStages], (uint32_t)((j / kKStages) & 1));
-    for (int j = n_vloads - kVStages < 0 ? 0 : n_vloads - kVStages; j < n_vloads; ++j)
-      (void)ptx::mbar_wait(&v_bar[j % kVStages], (uint32_t)((j / kVStages) & 1));
     if (n_mma1 > 0)
       (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
+  }
+  if (lead && aborted) {
+    for (int j = n_vloads - kVStages < 0 ? 0 : n_vloads - kVStages; j < n_vloads; ++j)
+      (void)ptx::mbar_wait(&v_bar[j % kVStages], (uint32_t)((j / kVStages) & 1));
     if (n_mma2 > 0)
       (void)ptx::mbar_wait(&o_bar[(n_mma2 - 1) & 1], (uint32_t)(((n_mma2 - 1) >> 1) & 1));
   }
