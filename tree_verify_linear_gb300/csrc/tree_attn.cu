@@ -74,8 +74,11 @@ constexpr int kSmemV = kSmemK + kKStages * kKBytes;
 constexpr int kSmemAnc = kSmemV + kVStages * kKBytes;      // uint64 [64]
 constexpr int kSmemRed = kSmemAnc + kMaxNodes * 8;        // float [2][128]
 constexpr int kSmemMisc = kSmemRed + 2 * kRows * 4;       // int [16]
-constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [9]
-constexpr int kSmemTotal = kSmemBars + 9 * 8;
+constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [13]
+constexpr int kSmemTotal = kSmemBars + 13 * 8;
+// threads: 8 softmax warps (two threads per row) and one issuing warp
+constexpr int kSoftmaxThreads = 2 * kRows;
+constexpr int kThreads = kSoftmaxThreads + 32;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory");
 static_assert(kSmemK % 1024 == 0 && kSmemV % 1024 == 0 && kKBytes % 1024 == 0,
               "swizzled operands");
@@ -158,7 +161,7 @@ __device__ __forceinline__ int blocks_of(const int32_t *ctx_len, int b) {
   return (ctx_len[b] + kKB - 1) / kKB + 1;
 }
 
-__global__ void __launch_bounds__(2 * kRows, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     tree_attn_kernel(const __grid_constant__ Maps maps, const Args A) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,15 +174,17 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   uint64_t *v_bar = k_bar + 3;                                        // [2]
   uint64_t *s_bar = k_bar + 5;                                        // [2]
   uint64_t *o_bar = k_bar + 7;                                        // [2]
+  uint64_t *s_free = k_bar + 9;   // [2] the softmax threads have read S (256 arrivals)
+  uint64_t *p_full = k_bar + 11;  // [2] the softmax threads have stored P (256 arrivals)
 
   // ---- whole-batch validation (the same verdict in every CTA) ----
   {
     int bad_in = 0;
-    for (int i = tid; i < Bq * N; i += 2 * kRows) {
+    for (int i = tid; i < Bq * N; i += kThreads) {
       const int n = i % N, p = A.parent[i];
       if (n == 0 ? p != -1 : (p < 0 || p >= n)) bad_in = 1;
     }
-    for (int i = tid; i < Bq; i += 2 * kRows)
+    for (int i = tid; i < Bq; i += kThreads)
       if (A.ctx_len[i] < 0 || A.ctx_len[i] > A.T) bad_in = 1;
     if (__syncthreads_or(bad_in)) {
       if (tid == 0 && A.status) *A.status = LBX_ETREE;
@@ -205,6 +210,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   // ---- set-up ----
   if (tid == 0) {
     for (int i = 0; i < 9; ++i) ptx::mbar_init(k_bar + i, 1);
+    for (int i = 9; i < 13; ++i) ptx::mbar_init(k_bar + i, kSoftmaxThreads);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -215,14 +221,13 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
-  const int quad = warp & 3, hf = warp >> 2;
+  const int quad = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quadrant
   const int r = quad * 32 + lane;
-  // two issuing threads in different warps: lead_s (warp 4) the S = Q K^T
-  // products and the K copies, lead (warp 0) the O += P V products and the
-  // V copies; each commit tracks its own thread's MMAs, and the two streams
-  // share no tensor memory
-  const bool lead = tid == 0, lead_s = tid == kRows;
+  // warps 0-7 run the softmax (two threads per row); lane 0 of warp 8 issues
+  // every copy and MMA and meets them through mbarriers only
+  const bool softmax = tid < kSoftmaxThreads;
+  const bool issuer = tid == kSoftmaxThreads;
 
   // descriptors of the Q tile and of stage 0; the others are fixed offsets
   // (added to the 16-byte address field)
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   // Blocks are numbered q = 0, 1, ... across this CTA's segments; stages,
   // buffers and mbarrier phases follow q.
   long long q0 = 0;
-  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by lead_s / lead
+  int n_kloads = 0, n_vloads = 0, n_mma1 = 0, n_mma2 = 0;  // issued by the issuer
   bool bad = false, aborted = false;
 
   // after an abort a CTA still walks its range, writing empty partials and
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     const int h0 = tile * g.hp;
     const int hp_t = g.G - h0 < g.hp ? g.G - h0 : g.hp;
     const int rows = hp_t * N;
-    const bool real_row = r < rows;
+    const bool real_row = softmax && r < rows;
     const int n_row = real_row ? r - (r / N) * N : 0;
 
     // ---- Q tile, ancestor masks (all of this segment's earlier MMAs are done) ----
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(2 * kRows, 1)
     }
     {
       const uint4 *qg = reinterpret_cast<const uint4 *>(A.q);
-      for (int idx = tid; idx < kRows * (kDh / 8); idx += 2 * kRows) {
+      for (int idx = tid; idx < kRows * (kDh / 8); idx += kThreads) {
         const int rr = idx / (kDh / 8), c16 = idx % (kDh / 8);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (rr < rows) {
@@ -361,157 +366,176 @@ __global__ void __launch_bounds__(2 * kRows, 1)
       ++n_mma2;
     };
 
-    if (lead_s && nb > 0) {
-      for (int i = 0; i < nb && i < kKStages; ++i) load_k(i);
-      if (!ptx::mbar_wait(&k_bar[q0 % kKStages], (uint32_t)((q0 / kKStages) & 1))) bad = true;
-      mma1(0);
-    }
-    if (lead && nb > 0)
-      for (int i = 0; i < nb && i < kVStages; ++i) load_v(i);
-
     float m_run = -INFINITY, l_run = 0.f;  // base-2 running max; this half's sum
-    for (int i = 0; i < nb; ++i) {
-      const long long q = q0 + i;
-      const bool tree_blk = blk0 + i == nctx;
-      // ---- this thread's 32 scores of the block ----
-      if (!ptx::mbar_wait(&s_bar[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
-      ptx::tc_fence_after();
-      float sv[kHalfKeys];
-      ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
-      ptx::tmem_wait_ld();
-      if (lead_s) {
-        // K of this block has been read (S is complete): its stage takes block i + 3
-        if (i + kKStages < nb) load_k(i + kKStages);
-        // the next block's scores, into the other buffer (read one block ago)
+    if (issuer) {
+      // ---- the issuing thread: copies and MMAs in block order ----
+      if (nb > 0) {
+        for (int i = 0; i < nb && i < kKStages; ++i) load_k(i);
+        for (int i = 0; i < nb && i < kVStages; ++i) load_v(i);
+        if (!ptx::mbar_wait(&k_bar[q0 % kKStages], (uint32_t)((q0 / kKStages) & 1))) bad = true;
+        if (!bad) mma1(0);
+      }
+      for (int i = 0; i < nb && !bad; ++i) {
+        const long long q = q0 + i;
+        // the next block's scores, into the other buffer once the softmax
+        // threads have read it (two blocks ago; earlier segments are done)
         if (i + 1 < nb) {
           if (!ptx::mbar_wait(&k_bar[(q + 1) % kKStages], (uint32_t)(((q + 1) / kKStages) & 1)))
             bad = true;
-          mma1(i + 1);
+          if (i >= 1 && !bad &&
+              !ptx::mbar_wait(&s_free[(q + 1) & 1], (uint32_t)(((q - 1) >> 1) & 1)))
+            bad = true;
+          if (!bad) mma1(i + 1);
         }
-      }
-      // ---- masked, scaled scores and the block maximum of the row ----
-      const int key0 = tree_blk ? 0 : (blk0 + i) * kKB;  // key (or node) of column 0
-      const int kend = tree_blk ? N : ctx;
-      const int kb = key0 + hf * kHalfKeys;  // this half's first key
-      float s2[kHalfKeys];
-      if (!tree_blk && kb + kHalfKeys <= kend) {
-#pragma unroll
-        for (int e = 0; e < kHalfKeys; ++e) s2[e] = sv[e] * A.scale_log2;
-      } else {
-#pragma unroll
-        for (int e = 0; e < kHalfKeys; ++e) {
-          const bool ok = tree_blk ? ((my_anc >> (kb + e)) & 1ull) != 0 : kb + e < kend;
-          s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
+        // K of this block is free once its S is complete: block i + 3 there
+        if (i + kKStages < nb) {
+          if (!bad && !ptx::mbar_wait(&s_bar[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
+          if (!bad) load_k(i + kKStages);
         }
-      }
-      float mx[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) mx[e] = fmaxf(s2[e], s2[e + 16]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
-      const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      red[hf * kRows + r] = mh;
-      // context keys past the cache's end: their V rows are zeroed, so that a
-      // non-finite value there cannot reach O through a zero weight
-      const int vrows = kend - key0;
-      if (!tree_blk && vrows < kKB && warp == 1) {
-        if (!ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1))) bad = true;
-        unsigned char *vd = smem + kSmemV + (int)(q % kVStages) * kKBytes;
-        const int zr = kKB - vrows;  // rows to clear, in each of the 4 atoms
-        for (int idx = lane; idx < (kDh / 64) * zr * 8; idx += 32) {
-          const int a = idx / (zr * 8), rm = idx - a * zr * 8;
-          *reinterpret_cast<uint4 *>(vd + a * kKVAtom + (vrows + rm / 8) * 128 + (rm % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        ptx::fence_proxy_async();
-      }
-      __syncthreads();  // -------------------------------------------- both halves' maxima
-      const float mb = fmaxf(mh, red[(1 - hf) * kRows + r]);
-      float alpha = 1.f;
-      bool need = false;
-      if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
-        alpha = ex2(m_run - mb);
-        need = i > 0;  // O holds earlier blocks (of both halves' keys)
-        l_run *= alpha;
-        m_run = mb;
-      }
-      // a row with no valid key yet (padding rows) takes 0 as its reference,
-      // so that masked keys weigh 2^-inf = 0
-      const float mref = m_run == -INFINITY ? 0.f : m_run;
-      float p[kHalfKeys];
-#pragma unroll
-      for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
-      float sm[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) sm[e] = p[e] + p[e + 16];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm[e] += sm[e + 8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
-      l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
-      // rows whose maximum moved rescale their half of O, once the previous
-      // P V product is done
-      if (__any_sync(0xffffffffu, need)) {
-        if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < kHalfCols / 32; ++c) {
-          const uint32_t col = tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c);
-          float ov[32];
-          ptx::tmem_ld32(col, ov);
-          ptx::tmem_wait_ld();
-          uint32_t w[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
-          ptx::tmem_st32(col, w);
-        }
-      }
-      // ---- P (bf16 hi and lo) -> TMEM ----
-      {
-        uint32_t ph[16], pl[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
-        const uint32_t pc = tq + kColP + (uint32_t)(q & 1) * kKB + hf * 16;
-        ptx::tmem_st16(pc, ph);
-        ptx::tmem_st16(pc + kKB / 2, pl);
-      }
-      // the lead: the previous P V product complete (O, its P buffer and its
-      // V stage free), then the next block's values into that stage
-      if (lead && i >= 1) {
-        if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
-        if (i + 1 < nb) load_v(i + 1);
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      if (__syncthreads_or(bad)) {  // ---------------------------------- P complete
-        aborted = true;
-        break;
-      }
-      if (lead) {
-        if (!ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1))) bad = true;
+        // this block's P, then O += P V
+        if (!bad && !ptx::mbar_wait(&p_full[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
+        if (!bad && !ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1)))
+          bad = true;
+        if (bad) break;
         ptx::tc_fence_after();
         mma2(i, i > 0);
+        // the previous product is done: its V stage takes block i + 1
+        if (i >= 1 && i + 1 < nb) {
+          if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
+          if (!bad) load_v(i + 1);
+        }
+      }
+    } else if (softmax) {
+      for (int i = 0; i < nb; ++i) {
+        const long long q = q0 + i;
+        const bool tree_blk = blk0 + i == nctx;
+        // ---- this thread's 32 scores of the block ----
+        if (!bad && !ptx::mbar_wait(&s_bar[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
+        ptx::tc_fence_after();
+        float sv[kHalfKeys];
+        ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&s_free[q & 1]);
+        // ---- masked, scaled scores and the block maximum of the row ----
+        const int key0 = tree_blk ? 0 : (blk0 + i) * kKB;  // key (or node) of column 0
+        const int kend = tree_blk ? N : ctx;
+        const int kb = key0 + hf * kHalfKeys;  // this half's first key
+        float s2[kHalfKeys];
+        if (!tree_blk && kb + kHalfKeys <= kend) {
+#pragma unroll
+          for (int e = 0; e < kHalfKeys; ++e) s2[e] = sv[e] * A.scale_log2;
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalfKeys; ++e) {
+            const bool ok = tree_blk ? ((my_anc >> (kb + e)) & 1ull) != 0 : kb + e < kend;
+            s2[e] = ok ? sv[e] * A.scale_log2 : -INFINITY;
+          }
+        }
+        float mx[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx[e] = fmaxf(s2[e], s2[e + 16]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], mx[e + 8]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], mx[e + 4]);
+        const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        red[hf * kRows + r] = mh;
+        // context keys past the cache's end: their V rows are zeroed, so that a
+        // non-finite value there cannot reach O through a zero weight
+        const int vrows = kend - key0;
+        if (!tree_blk && vrows < kKB && warp == 1) {
+          if (!bad && !ptx::mbar_wait(&v_bar[q % kVStages], (uint32_t)((q / kVStages) & 1)))
+            bad = true;
+          unsigned char *vd = smem + kSmemV + (int)(q % kVStages) * kKBytes;
+          const int zr = kKB - vrows;  // rows to clear, in each of the 4 atoms
+          for (int idx = lane; idx < (kDh / 64) * zr * 8; idx += 32) {
+            const int a = idx / (zr * 8), rm = idx - a * zr * 8;
+            *reinterpret_cast<uint4 *>(vd + a * kKVAtom + (vrows + rm / 8) * 128 + (rm % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          ptx::fence_proxy_async();
+        }
+        ptx::named_sync(1, kSoftmaxThreads);  // ---------------- both halves' maxima
+        const float mb = fmaxf(mh, red[(1 - hf) * kRows + r]);
+        float alpha = 1.f;
+        bool need = false;
+        if (mb > m_run + 8.f) {  // move the reference maximum (also the first time)
+          alpha = ex2(m_run - mb);
+          need = i > 0;  // O holds earlier blocks (of both halves' keys)
+          l_run *= alpha;
+          m_run = mb;
+        }
+        // a row with no valid key yet (padding rows) takes 0 as its reference,
+        // so that masked keys weigh 2^-inf = 0
+        const float mref = m_run == -INFINITY ? 0.f : m_run;
+        float p[kHalfKeys];
+#pragma unroll
+        for (int e = 0; e < kHalfKeys; ++e) p[e] = ex2(s2[e] - mref);
+        float sm[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sm[e] = p[e] + p[e + 16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sm[e] += sm[e + 8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sm[e] += sm[e + 4];
+        l_run += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+        // rows whose maximum moved rescale their half of O, once the previous
+        // P V product is done
+        if (__any_sync(0xffffffffu, need)) {
+          if (!bad && !ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1)))
+            bad = true;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kHalfCols / 32; ++c) {
+            const uint32_t col = tq + kColO + (uint32_t)(hf * kHalfCols + 32 * c);
+            float ov[32];
+            ptx::tmem_ld32(col, ov);
+            ptx::tmem_wait_ld();
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
+            ptx::tmem_st32(col, w);
+          }
+        }
+        // ---- P (bf16 hi and lo) -> TMEM, once its buffer's last product
+        // (two blocks ago; earlier segments are done) has completed ----
+        if (i >= 2 && !bad &&
+            !ptx::mbar_wait(&o_bar[(q - 2) & 1], (uint32_t)(((q - 2) >> 1) & 1)))
+          bad = true;
+        ptx::tc_fence_after();
+        {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
+          const uint32_t pc = tq + kColP + (uint32_t)(q & 1) * kKB + hf * 16;
+          ptx::tmem_st16(pc, ph);
+          ptx::tmem_st16(pc + kKB / 2, pl);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&p_full[q & 1]);
       }
     }
 
     // ---- this segment's partial -> workspace (slot (CTA group + KV group)
     // x tiles + tile, unique since along the list either advances by one) ----
-    if (!aborted && nb > 0) {
+    if (softmax && nb > 0 && !bad) {
       const long long ql = q0 + nb - 1;
       if (!ptx::mbar_wait(&o_bar[ql & 1], (uint32_t)((ql >> 1) & 1))) bad = true;
     }
     ptx::tc_fence_after();
-    red[hf * kRows + r] = l_run;
-    __syncthreads();
-    const bool valid = !aborted && !bad;
+    if (softmax) red[hf * kRows + r] = l_run;
+    // a wait that timed out anywhere in the CTA ends its work (empty partials
+    // from here on, so that every counter still completes)
+    if (__syncthreads_or(bad)) aborted = true;
+    const bool valid = !aborted;
     float *pp = A.part + (size_t)((cg + kvg) * tiles + tile) * unit_floats(g);
     if (real_row && hf == 0) {
       pp[r] = valid && nb > 0 ? m_run : -INFINITY;
       pp[kRows + r] = valid && nb > 0 ? red[r] + red[kRows + r] : 0.f;
     }
-    if (valid && nb > 0 && quad * 32 < rows) {
+    if (valid && nb > 0 && softmax && quad * 32 < rows) {
       float *orow = pp + 2 * kRows + (size_t)r * kDh + hf * kHalfCols;
 #pragma unroll 1
       for (int c = 0; c < kHalfCols / 32; ++c) {
@@ -590,15 +614,13 @@ __global__ void __launch_bounds__(2 * kRows, 1)
   }
 
   // ---- drain: copies and MMAs still in flight after an abort ----
-  if (lead_s && aborted) {
+  if (issuer && aborted) {
     for (int j = n_kloads - kKStages < 0 ? 0 : n_kloads - kKStages; j < n_kloads; ++j)
       (void)ptx::mbar_wait(&k_bar[j % kKStages], (uint32_t)((j / kKStages) & 1));
-    if (n_mma1 > 0)
-      (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
-  }
-  if (lead && aborted) {
     for (int j = n_vloads - kVStages < 0 ? 0 : n_vloads - kVStages; j < n_vloads; ++j)
       (void)ptx::mbar_wait(&v_bar[j % kVStages], (uint32_t)((j / kVStages) & 1));
+    if (n_mma1 > 0)
+      (void)ptx::mbar_wait(&s_bar[(n_mma1 - 1) & 1], (uint32_t)(((n_mma1 - 1) >> 1) & 1));
     if (n_mma2 > 0)
       (void)ptx::mbar_wait(&o_bar[(n_mma2 - 1) & 1], (uint32_t)(((n_mma2 - 1) >> 1) & 1));
   }
@@ -706,6 +728,6 @@ extern "C" int lbx_tree_attention(int L, int Bq, int N, int Hq, int Hkv, int dh,
   int grid = nsm < kMaxCtas ? nsm : kMaxCtas;
   grid = grid / A.geo.tiles * A.geo.tiles;
   if (grid < A.geo.tiles) grid = A.geo.tiles;
-  tree_attn_kernel<<<(unsigned)grid, 2 * kRows, kSmemTotal, stream>>>(maps, A);
+  tree_attn_kernel<<<(unsigned)grid, kThreads, kSmemTotal, stream>>>(maps, A);
   return cudaGetLastError() == cudaSuccess ? LBX_OK : LBX_ECUDA;
 }
