@@ -143,6 +143,12 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uin
   lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
+// One plain arrival on an mbarrier (release semantics for this thread's
+// earlier memory operations).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
+}
+
 // 2^x on the hardware exponential unit (x <= 0 here; -inf gives 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&s_free[q & 1]);
+        mbar_arrive(&s_free[q & 1]);
         // ---- masked, scaled scores and the block maximum of the row ----
         const int key0 = tree_blk ? 0 : (blk0 + i) * kKB;  // key (or node) of column 0
         const int kend = tree_blk ? N : ctx;
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&p_full[q & 1]);
+        mbar_arrive(&p_full[q & 1]);
       }
     }
 
