@@ -66,15 +66,15 @@ __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / 
 // an SM (256 TMEM columns and at most 113 KB of shared memory each); larger
 // capacities (up to 64) take one CTA per SM with all 512 TMEM columns.  The
 // prep kernel handles prep_heads value heads at a time (its per-head scratch
-// grows with NMAX^2); at the large capacities its shared memory allows one
-// CTA per SM, which then runs 16 warps.
+// grows with NMAX^2); at the large capacities two of its 16-warp CTAs share
+// an SM (64 registers per thread, at most 113 KB of shared memory each).
 template <int NMAX>
 struct TcRes {
   static constexpr int ctas = NMAX <= 24 ? 2 : 1;
   static constexpr uint32_t tmem_cols = NMAX <= 24 ? 256u : 512u;
   static constexpr int max_smem = NMAX <= 24 ? 113 * 1024 : 227 * 1024;
-  static constexpr int prep_ctas = NMAX <= 24 ? 4 : 1;
-  static constexpr int prep_heads = NMAX <= 24 ? 4 : 2;
+  static constexpr int prep_ctas = NMAX <= 24 ? 4 : 2;
+  static constexpr int prep_heads = NMAX <= 24 ? 4 : 3;
   static constexpr int prep_threads = NMAX <= 24 ? 256 : 512;
 };
 
@@ -188,32 +188,47 @@ struct TcLayout {
   static_assert(stg % 128 == 0 && tb % 16 == 0 && hr % 16 == 0 && b2hi % 16 == 0, "alignment");
 };
 
-// Shared memory of the prep kernel (one CTA per key head).  After the conv
-// the staged inputs are dead and the same bytes hold the per-head T scratch
-// and gate vectors of up to kPrepHeads value heads at a time.
+// Shared memory of the prep kernel (one CTA per key head).  Up to 24 nodes
+// (four CTAs per SM, bound by registers): staged q and k inputs, fp32 rows,
+// Gram entries, tables; after the Gram the staging bytes hold the per-head
+// T scratch and gate vectors of up to kPrepHeads value heads at a time.  At
+// the large capacities (kCompact: two CTAs per SM, bound by shared memory)
+// the regions are reused by phase:
+//   * conv: staged q inputs in sq, the staged k inputs in the bytes of the q
+//     rows of kqf (the k conv runs first, the q conv then overwrites them);
+//     the accepted node's new conv window is kept aside in nw;
+//   * after the conv: the Gram entries in sq, the fp32 rows still in kqf;
+//   * after the Gram: the per-head scratch in kqf.
 template <int NMAX>
 struct PrepLayout {
   static constexpr int kPrepHeads = TcRes<NMAX>::prep_heads;
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
   static constexpr int NP = round_up(NMAX, 4);
-  static constexpr int sq = 0;                        // staged q inputs
-  static constexpr int sk = sq + CS::bytes;           // staged k inputs
-  // reuse of the staging bytes, per head chunk
-  static constexpr int tf = 0;                        // float [kPrepHeads][NMAX][TP]
+  static constexpr int KQP = kTcD + 4;                 // padded row pitch (bank spread)
+  static constexpr int kRows = Ly::NC * KQP * 4;       // fp32 [NC][KQP]: k rows, then q rows
+  static constexpr bool kCompact = TcRes<NMAX>::prep_ctas == 2;
+  static_assert(!kCompact || CS::bytes <= NMAX * KQP * 4, "staged k inputs fit the q rows");
+  static constexpr int sq = 0;                         // staged q inputs
+  static constexpr int kqf = kCompact ? sq + CS::bytes : sq + 2 * CS::bytes;
+  static constexpr int sk = kCompact ? kqf + NMAX * KQP * 4 : sq + CS::bytes;  // staged k inputs
+  static constexpr int gr = kCompact ? sq : kqf + kRows;  // Gram entries
+  static_assert(!kCompact || GramLayout<NMAX>::bytes <= CS::bytes, "Gram entries fit the staging");
+  // per head chunk, after the Gram
+  static constexpr int tf = kCompact ? kqf : 0;       // float [kPrepHeads][NMAX][TP]
   static constexpr int han = tf + kPrepHeads * NMAX * Ly::TP * 4;  // float [kPrepHeads][NP]
   static constexpr int hbn = han + kPrepHeads * NP * 4;
   static constexpr int hgam = hbn + kPrepHeads * NP * 4;
-  static_assert(hgam + kPrepHeads * NP * 4 <= 2 * CS::bytes, "head scratch fits the staging");
-  static constexpr int KQP = kTcD + 4;               // padded row pitch (bank spread)
-  static constexpr int kqf = sk + CS::bytes;          // fp32 [NC][KQP]: k rows, then q rows
-  static constexpr int gr = kqf + Ly::NC * KQP * 4;   // Gram entries
-  static constexpr int tb = gr + GramLayout<NMAX>::bytes;
-  static constexpr int porig = tb + TabLayout<NMAX>::bytes;  // int [NMAX] input parents
+  static_assert(hgam + kPrepHeads * NP * 4 <= (kCompact ? kqf + kRows : 2 * CS::bytes),
+                "head scratch fits");
+  static constexpr int tb = kCompact ? kqf + kRows : gr + GramLayout<NMAX>::bytes;
+  static constexpr int nw = tb + TabLayout<NMAX>::bytes;  // float [2][K-1][128]: q, k
+  static constexpr int porig = nw + (kCompact ? 2 * (LBX_MAX_CONV_WIDTH - 1) * kTcD * 4 : 0);
   static constexpr int misc = porig + 4 * NP;
   static constexpr int bar = (misc + 64 + 7) & ~7;
   static constexpr int total = bar + 8;
   static_assert(sq % 128 == 0 && sk % 128 == 0, "TMA destinations");
+  static_assert(total + 1024 <= 233472 / TcRes<NMAX>::prep_ctas, "prep CTAs per SM");
 };
 
 // Workspace layout of the tensor-core step: the tree tables of every

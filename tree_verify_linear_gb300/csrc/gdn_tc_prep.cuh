@@ -352,23 +352,33 @@ __global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_c
   __syncthreads();
 
   // Warp 0 builds the request's tree tables and checks the batch while warps
-  // 1..7 run the q, then k conv + SiLU + L2 norm of every node (input
-  // labels, windows walked along the parents) into fp32 rows.
+  // 1.. run the q and k conv + SiLU + L2 norm of every node (input labels,
+  // windows walked along the parents) into fp32 rows.  In the compact layout
+  // the k conv runs first (its staged inputs sit in the q rows) and the
+  // accepted node's window is kept aside: its K-1 newest raw inputs become
+  // the slot's new conv window, written once the batch is known to be valid,
+  // after the staged inputs are gone.
   int code = 0;
+  float *nwin = reinterpret_cast<float *>(smem + PL::nw);
   if (warp == 0) {
     build_tables_warp<NMAX>(tid, N, K, A.accepted[bq], A.parent + (size_t)bq * N, tb);
     code = validate_batch(A.parent, A.slot, A.accepted, Bq, N, A.n_slots, false, true, true,
                           tid, 32);
-  } else if (!ptx::mbar_wait(bar, 0)) {
-    code = LBX_ETIMEOUT;
   } else {
+    // one verdict per warp (the conv below runs whole-warp shuffles)
+    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar, 0));
+    if (!ok) code = LBX_ETIMEOUT;
     constexpr int CT = kPrepThreads - 32;  // conv threads
     constexpr int GQ = kTcD / 8;           // 16 threads per node, 8 channels each
     constexpr int U = (NMAX * GQ + CT - 1) / CT;
     static_assert(CT % GQ == 0, "channel group fixed per thread");
     const int ct = tid - 32, li = ct % GQ;
+    const int acc = A.accepted[bq];
 #pragma unroll 1
-    for (int which = 0; which < 2; ++which) {
+    for (int pass = 0; pass < 2; ++pass) {
+      const int which = PL::kCompact ? 1 - pass : pass;  // 0: q, 1: k
+      if (PL::kCompact && pass == 1) ptx::named_sync(1, CT);  // staged k inputs consumed
+      if (!ok) continue;
       const unsigned char *cs = which == 0 ? sq : sk;
       float wsl[8][LBX_MAX_CONV_WIDTH];
       conv_weights8<NMAX>(wsl, K, cs, li * 8);
@@ -423,6 +433,43 @@ __global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_c
           kd[1] = make_float4(scale * v8[4], scale * v8[5], scale * v8[6], scale * v8[7]);
         }
       }
+      if (PL::kCompact && ct < GQ && acc >= 0 && acc < N) {
+        // the slot's new conv window, oldest row first: row rr is window
+        // element K-2-rr of the accepted node (raw inputs, copied exactly)
+        int w[LBX_MAX_CONV_WIDTH - 1];
+        {
+          int m = acc, past = 0;
+#pragma unroll
+          for (int j = 0; j < LBX_MAX_CONV_WIDTH - 1; ++j) {
+            if (m >= 0) {
+              w[j] = m;
+              m = porig[m];
+            } else {
+              ++past;
+              w[j] = -1 - (K - 1 - past);
+            }
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr) {
+          if (rr >= K - 1) break;
+          const int j = K - 2 - rr;
+          const int wr = j == 0 ? w[0] : (j == 1 ? w[1] : w[2]);
+          float4 *dst = reinterpret_cast<float4 *>(
+              nwin + (which * (LBX_MAX_CONV_WIDTH - 1) + rr) * kTcD + ct * 8);
+          if (wr >= 0) {
+            float xv[8];
+            unpack8(*reinterpret_cast<const uint4 *>(cs + CS::x + wr * kTcD * 2 + ct * 16), xv);
+            dst[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+            dst[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+          } else {
+            const float4 *cp =
+                reinterpret_cast<const float4 *>(cs + CS::c + (-1 - wr) * kTcD * 4 + ct * 32);
+            dst[0] = cp[0];
+            dst[1] = cp[1];
+          }
+        }
+      }
     }
   }
   // one barrier: conv rows and tables written, and the block's verdict
@@ -435,7 +482,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_c
     }
     return;
   }
-  const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
   const int *dep = reinterpret_cast<const int *>(tb + TL::dep);
   const int *off = reinterpret_cast<const int *>(tb + TL::off);
   const int *off2 = reinterpret_cast<const int *>(tb + TL::off2);
@@ -467,16 +513,23 @@ __global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_c
   }
   if (tid < 2 * kTcD) {
     // new conv window of the key head's q (threads 0..127) and k (128..255)
-    // channels, from the staged old window and inputs
+    // channels: kept aside during the conv (compact layout), else from the
+    // staged old window and inputs
     const int which = tid >> 7, c = tid & (kTcD - 1);
-    const unsigned char *cs = which == 0 ? sq : sk;
-    const uint16_t *xs = reinterpret_cast<const uint16_t *>(cs + CS::x);
-    const float *cc = reinterpret_cast<const float *>(cs + CS::c);
     float *cache_o = A.conv_cache_out + ((size_t)l * A.n_slots + slot_b) * (K - 1) * C;
     const int gc = (which * Hk + kh) * kTcD + c;
-    for (int rr = 0; rr < K - 1; ++rr) {
-      const int w = crow[rr];
-      cache_o[(size_t)rr * C + gc] = w >= 0 ? bf2f(xs[w * kTcD + c]) : cc[(-1 - w) * kTcD + c];
+    if (PL::kCompact) {
+      for (int rr = 0; rr < K - 1; ++rr)
+        cache_o[(size_t)rr * C + gc] = nwin[(which * (LBX_MAX_CONV_WIDTH - 1) + rr) * kTcD + c];
+    } else {
+      const int *crow = reinterpret_cast<const int *>(tb + TL::crow);
+      const unsigned char *cs = which == 0 ? sq : sk;
+      const uint16_t *xs = reinterpret_cast<const uint16_t *>(cs + CS::x);
+      const float *cc = reinterpret_cast<const float *>(cs + CS::c);
+      for (int rr = 0; rr < K - 1; ++rr) {
+        const int w = crow[rr];
+        cache_o[(size_t)rr * C + gc] = w >= 0 ? bf2f(xs[w * kTcD + c]) : cc[(-1 - w) * kTcD + c];
+      }
     }
   }
   {
