@@ -105,7 +105,7 @@ int launch_tc(const StepArgs &A, void *ws, size_t ws_bytes, cudaStream_t st) {
   // prep kernel's last CTAs run, and waits for it before reading the workspace
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid);
-  lc.blockDim = dim3(kTcThreads);
+  lc.blockDim = dim3(TcRes<NMAX>::threads);
   lc.dynamicSmemBytes = smem;
   lc.stream = st;
   cudaLaunchAttribute attr[1];

@@ -1,10 +1,12 @@
 // gdn_tc.cuh -- fused tree-verify step on tensor cores (sm_103a, d = 128).
 //
-// Two CTAs share each SM (at most 113 KB of shared memory and 256 TMEM
-// columns each), so the latency-bound phases of one CTA overlap the other's.
-// A CTA has 8 warps; warps w and w + 4 share TMEM lane quadrant w, and each
-// state row (= TMEM lane) has two threads, one per half: of the 128 columns
-// when the state is split and written back, of the nodes in the row work.
+// Up to 24 nodes two CTAs share each SM (at most 113 KB of shared memory and
+// 256 TMEM columns each), so the latency-bound phases of one CTA overlap the
+// other's; a CTA has 8 warps, warps w and w + 4 share TMEM lane quadrant w,
+// and each state row (= TMEM lane) has two threads, one per part: of the 128
+// columns when the state is split and written back, of the nodes in the row
+// work.  Larger capacities take one CTA of 16 warps per SM and four parts
+// (warps w, w + 4, w + 8, w + 12 on quadrant w).
 // The work is a list of tiles, one per (layer l, request b, value head h) =
 // one 128 x 128 fp32 state slab, ordered (l, b, key head, head in group);
 // every CTA takes a contiguous range, so consecutive tiles usually share
@@ -62,9 +64,11 @@ constexpr int kTcMaxSmem = 113 * 1024;             // two CTAs per SM
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Resources of the tree step by node capacity: up to 24 nodes two CTAs share
-// an SM (256 TMEM columns and at most 113 KB of shared memory each); larger
-// capacities (up to 64) take one CTA per SM with all 512 TMEM columns.  The
+// Resources of the tree step by node capacity: up to 24 nodes two CTAs of 8
+// warps share an SM (256 TMEM columns and at most 113 KB of shared memory
+// each), with two threads per state row; larger capacities (up to 64) take
+// one CTA of 16 warps per SM with all 512 TMEM columns, four threads per
+// state row (parts: each has a quarter of the nodes and columns).  The
 // prep kernel handles prep_heads value heads at a time (its per-head scratch
 // grows with NMAX^2); at the large capacities two of its 16-warp CTAs share
 // an SM (64 registers per thread, at most 113 KB of shared memory each).
@@ -76,6 +80,8 @@ struct TcRes {
   static constexpr int prep_ctas = NMAX <= 24 ? 4 : 2;
   static constexpr int prep_heads = NMAX <= 24 ? 4 : 3;
   static constexpr int prep_threads = NMAX <= 24 ? 256 : 512;
+  static constexpr int parts = NMAX <= 24 ? 2 : 4;  // threads per state row
+  static constexpr int threads = 128 * parts;
 };
 
 // Staged conv inputs of one 128-channel block for N nodes: raw inputs
@@ -177,7 +183,8 @@ struct TcLayout {
   static constexpr int hr = tb + TabLayout<NMAX>::bytes;  // value-head record
   // v values of the lead warp's rows for its last kVOff nodes, computed by
   // warps 1..kVOff (float [kVOff][32])
-  static constexpr int kVOff = NMAX / 4 < 7 ? NMAX / 4 : 7;
+  static constexpr int kVOff =
+      NMAX / TcRes<NMAX>::parts / 2 < 7 ? NMAX / TcRes<NMAX>::parts / 2 : 7;
   static constexpr int vx = hr + HeadLayout<NMAX>::bytes;
   static constexpr int misc = vx + kVOff * 128;  // ints, see kernel
   static constexpr int bars = (misc + 64 + 7) & ~7;   // 6 x uint64
@@ -423,20 +430,32 @@ __device__ __forceinline__ void persist_channel_global(int gc, int K, int C, con
     if (rr < K - 1) cache_out[(size_t)rr * C + gc] = val[rr];
 }
 
-// Node values of half HF of a row (NMAX / 2 nodes), as packed bf16 pairs,
-// hi and lo, into the A columns of MMA2 / MMA3 (hi at a2, lo at a2 + KP/2):
-// half 0 writes pairs 0 .. C0-1, half 1 pairs C0 .. KP/2-1 (its nodes, then
-// the zero padding up to KP).
+// Calls f(integral_constant<part>) for the run-time part index p < PARTS.
+template <int PARTS, class F>
+__device__ __forceinline__ void by_part(int p, F &&f) {
+  if (p == 0) f(std::integral_constant<int, 0>{});
+  else if (p == 1) f(std::integral_constant<int, 1>{});
+  else if constexpr (PARTS > 2) {
+    if (p == 2) f(std::integral_constant<int, 2>{});
+    else f(std::integral_constant<int, 3>{});
+  }
+}
+
+// Node values of part HF of a row (NMAX / parts nodes), as packed bf16
+// pairs, hi and lo, into the A columns of MMA2 / MMA3 (hi at a2, lo at
+// a2 + KP/2): part p writes the pairs of its nodes, the last part also the
+// zero padding up to KP.
 template <int NMAX, int HF>
 __device__ __forceinline__ void store_pairs(uint32_t a2, const float *v) {
   using Ly = TcLayout<NMAX>;
-  constexpr int NH = NMAX / 2, KP = Ly::KP, KH = KP / 2;
-  constexpr int C0 = NH / 2, C1 = (NH + KP - NMAX) / 2;
-  constexpr int CNT = HF ? C1 : C0, OFF = HF ? C0 : 0;
+  constexpr int PARTS = TcRes<NMAX>::parts;
+  constexpr int NQ = NMAX / PARTS, KP = Ly::KP, KH = KP / 2;
+  // the last part also zero-fills the padding columns up to KP
+  constexpr int CNT = HF < PARTS - 1 ? NQ / 2 : (NQ + KP - NMAX) / 2, OFF = HF * NQ / 2;
   uint32_t ph[CNT], pl[CNT];
 #pragma unroll
   for (int e = 0; e < CNT; ++e)
-    split_bf16x2(2 * e < NH ? v[2 * e] : 0.f, 2 * e + 1 < NH ? v[2 * e + 1] : 0.f, ph[e], pl[e]);
+    split_bf16x2(2 * e < NQ ? v[2 * e] : 0.f, 2 * e + 1 < NQ ? v[2 * e + 1] : 0.f, ph[e], pl[e]);
   ptx::tmem_st_run<OFF, CNT>(a2, ph);
   ptx::tmem_st_run<OFF, CNT>(a2 + KH, pl);
 }
@@ -463,8 +482,9 @@ __device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t a, uint32_t b1)
 }
 
 template <int NMAX>
-__global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
+__global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     gdn_step_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs T) {
+  constexpr int NT = TcRes<NMAX>::threads, PARTS = TcRes<NMAX>::parts;
   using Ly = TcLayout<NMAX>;
   using CS = ConvStage<NMAX>;
   constexpr int NC = Ly::NC, R1 = Ly::R1, KP = Ly::KP, KH = KP / 2;
@@ -654,15 +674,17 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
     load_hr(t_begin);
   }
 
-  // state row r (= TMEM lane) and half hf of this thread; the row work of
-  // nodes n0 .. n0 + NH - 1 is this thread's
-  const int quad = warp & 3, hf = warp >> 2;
+  // state row r (= TMEM lane) and part pt of this thread; the row work of
+  // nodes n0 .. n0 + NQ - 1 and of state columns pt * CPP .. + CPP - 1 is
+  // this thread's
+  const int quad = warp & 3, pt = warp >> 2;
   const int r = quad * 32 + (tid & 31);
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
-  constexpr int NH = NMAX / 2;                        // nodes per half
-  static_assert(NH % 2 == 0, "node halves");
-  const int n0 = hf * NH;
-  constexpr int LB = NH <= 4 ? 4 : 8;  // accumulator columns per TMEM load
+  constexpr int NQ = NMAX / PARTS;                    // nodes per part
+  constexpr int CPP = kTcD / PARTS;                   // state columns per part
+  static_assert(NQ % 2 == 0 && CPP % 32 == 0, "node pairs, 32-column TMEM runs");
+  const int n0 = pt * NQ;
+  constexpr int LB = NQ <= 4 ? 4 : 8;  // accumulator columns per TMEM load
 
   int cur_req = -1, cur_group = -1;
   for (int it = 0; it < count; ++it) {
@@ -679,7 +701,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
     if (bq != cur_req) {
       cur_req = bq;
       // [T | W] entries outside the (node, ancestor-or-self) pairs stay zero
-      for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += kTcThreads)
+      for (int idx = tid; idx < 2 * Ly::kB2 / 16; idx += NT)
         *reinterpret_cast<uint4 *>(B2hi + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
       wait_on(tab_bar, tab_waits);
     }
@@ -690,11 +712,11 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
 
     // ================= [T | W] of this value head =================
     wait_on(hr_bar, hr_waits);
-    ptx::named_sync(1, kTcThreads);  // zero-filled [T|W] (new request) before the scatter
+    ptx::named_sync(1, NT);  // zero-filled [T|W] (new request) before the scatter
     const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
     {
       const int nl = meta[1];
-      for (int lane = tid; lane < nl; lane += kTcThreads) {
+      for (int lane = tid; lane < nl; lane += NT) {
         const uint32_t o = lofs[lane];
         uint16_t th, tl, wh, wl;
         split_bf16(tw[lane], th, tl);
@@ -713,18 +735,23 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
       bad = true;
     }
     {
-      // this thread's 64 columns of the row: hi into A columns hf*32.., lo
-      // into 64 + hf*32..
-      uint32_t vh[32], vl[32];
+      // this thread's CPP columns of the row: hi into A columns pt * CPP / 2
+      // .., lo 64 columns further
+      uint32_t vh[CPP / 2], vl[CPP / 2];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < CPP / 4; ++q) {
         const float4 x4 =
-            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, hf * 64 + 4 * q));
+            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, pt * CPP + 4 * q));
         split_bf16x2(x4.x, x4.y, vh[2 * q], vl[2 * q]);
         split_bf16x2(x4.z, x4.w, vh[2 * q + 1], vl[2 * q + 1]);
       }
-      ptx::tmem_st32(tq + Ly::cA1 + hf * 32, vh);
-      ptx::tmem_st32(tq + Ly::cA1 + 64 + hf * 32, vl);
+      if constexpr (CPP == 64) {
+        ptx::tmem_st32(tq + Ly::cA1 + pt * 32, vh);
+        ptx::tmem_st32(tq + Ly::cA1 + 64 + pt * 32, vl);
+      } else {
+        ptx::tmem_st16(tq + Ly::cA1 + pt * 16, vh);
+        ptx::tmem_st16(tq + Ly::cA1 + 64 + pt * 16, vl);
+      }
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
@@ -742,11 +769,12 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
 
     // ================= v of this row for this half's nodes (staged inputs) =================
     // The lead warp (warp 0) has just issued MMA1, so it computes only its
-    // first NH - kVOff nodes; warps 1..kVOff each compute one of its other
+    // first NQ - kVOff nodes; warps 1..kVOff each compute one of its other
     // nodes for its 32 rows and pass the values through shared memory.
     wait_on(stg_bar, stg_waits);
-    float vv[NH];
-    constexpr int kVOff = Ly::kVOff, kVOwn = NH - kVOff;
+    float vv[NQ];
+    constexpr int kVOff = Ly::kVOff, kVOwn = NQ - kVOff;
+    static_assert(kVOwn > 0 && kVOff < NT / 32, "v conv offload");
     float *vx = reinterpret_cast<float *>(smem + Ly::vx);
     {
       const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
@@ -778,7 +806,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
         for (int i = 0; i < kVOwn; ++i) vv[i] = vconv(n0 + i, r, wslot);
       } else {
 #pragma unroll
-        for (int i = 0; i < NH; ++i) vv[i] = vconv(n0 + i, r, wslot);
+        for (int i = 0; i < NQ; ++i) vv[i] = vconv(n0 + i, r, wslot);
         if (warp <= kVOff) {
           const int lane = tid & 31;
           float w0[LBX_MAX_CONV_WIDTH];
@@ -787,7 +815,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
         }
       }
       // this row's value channel of the conv window (only this tile reads it)
-      if (hf == 0) {
+      if (pt == 0) {
 #pragma unroll
         for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
           if (rr < K - 1) {
@@ -797,28 +825,28 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
           }
       }
     }
-    ptx::named_sync(1, kTcThreads);  // staging consumed
+    ptx::named_sync(1, NT);  // staging consumed
     if (lead && it + 1 < count) load_block(nx);
     if (warp == 0) {
 #pragma unroll
-      for (int i = kVOwn; i < NH; ++i) vv[i] = vx[(i - kVOwn) * 32 + (tid & 31)];
+      for (int i = kVOwn; i < NQ; ++i) vv[i] = vx[(i - kVOwn) * 32 + (tid & 31)];
     }
 
     // ================= rhs -> tensor memory =================
     // Accumulator columns are read in aligned blocks of LB covering this
-    // half's nodes; node N0 + i sits at position SH + i of the block.
+    // part's nodes; node N0 + i sits at position SH + i of the block.
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
-    float oq[NH];
+    float oq[NQ];
     auto rhs_half = [&](auto hfc) {
       constexpr int HF = decltype(hfc)::value;
-      constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
-      constexpr int NL = round_up(SH + NH, LB);
+      constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
+      constexpr int NL = round_up(SH + NQ, LB);
       // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
-      float rhs[NH];
+      float rhs[NQ];
       // accumulator columns in pieces of CH * LB (all at once for small
       // halves; 8 columns at a time for the large ones, to bound registers)
-      constexpr int CH = NH > 12 ? 1 : NL / LB;
+      constexpr int CH = NQ > 12 ? 1 : NL / LB;
       static_assert(CH == NL / LB || SH == 0, "chunked halves start aligned");
 #pragma unroll
       for (int c0 = 0; c0 < NL / LB; c0 += CH) {
@@ -835,7 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
 #pragma unroll
         for (int e = 0; e < CH * LB; ++e) {
           const int i = c0 * LB + e - SH;  // node N0 + i
-          if (i >= 0 && i < NH) {
+          if (i >= 0 && i < NQ) {
             const int n = N0 + i;
             const float ag = an[n] * gam[n];
             rhs[i] = bn[n] * fmaf(-ag, k_hi[e] + k_lo[e], vv[i]);
@@ -845,15 +873,12 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, rhs);
     };
-    if (hf == 0)
-      rhs_half(std::integral_constant<int, 0>{});
-    else
-      rhs_half(std::integral_constant<int, 1>{});
+    by_part<PARTS>(pt, rhs_half);
     // gamma_acc S0 into the MMA3 accumulator (the S0 columns, free since
-    // MMA1 completed), this thread's 64 columns; the stage is not read again
+    // MMA1 completed), this thread's columns; the stage is not read again
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int k0 = 64 * hf + 32 * c;
+    for (int c = 0; c < CPP / 32; ++c) {
+      const int k0 = CPP * pt + 32 * c;
       uint32_t gs[32];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -898,11 +923,11 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
     ptx::tc_fence_after();
     auto od_half = [&](auto hfc) {
       constexpr int HF = decltype(hfc)::value;
-      constexpr int N0 = HF * NH, B0 = N0 / LB * LB, SH = N0 - B0;
-      constexpr int NL = round_up(SH + NH, LB);
-      constexpr int CH = NH > 12 ? 1 : NL / LB;
+      constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
+      constexpr int NL = round_up(SH + NQ, LB);
+      constexpr int CH = NQ > 12 ? 1 : NL / LB;
       float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
-      float dl[NH];
+      float dl[NQ];
 #pragma unroll
       for (int c0 = 0; c0 < NL / LB; c0 += CH) {
         float dd[CH * LB], wr[CH * LB];
@@ -916,7 +941,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
 #pragma unroll
         for (int e = 0; e < CH * LB; ++e) {
           const int i = c0 * LB + e - SH;  // node N0 + i
-          if (i >= 0 && i < NH) {
+          if (i >= 0 && i < NQ) {
             const int n = N0 + i;
             if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[i] + wr[e]);
             dl[i] = cpa[n] * dd[e];
@@ -925,10 +950,7 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, dl);
     };
-    if (hf == 0)
-      od_half(std::integral_constant<int, 0>{});
-    else
-      od_half(std::integral_constant<int, 1>{});
+    by_part<PARTS>(pt, od_half);
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     if (__syncthreads_or(bad)) {  // ---------------------------------------------- S3
@@ -971,10 +993,10 @@ __global__ void __launch_bounds__(kTcThreads, TcRes<NMAX>::ctas)
     {
       float *srow =
           A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD;
-      // this thread's 64 columns, 32 at a time
+      // this thread's columns, 32 at a time
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int k0 = 64 * hf + 32 * c;
+      for (int c = 0; c < CPP / 32; ++c) {
+        const int k0 = CPP * pt + 32 * c;
         float d[32];
         ptx::tmem_ld32(tq + Ly::cA1 + k0, d);
         ptx::tmem_wait_ld();
