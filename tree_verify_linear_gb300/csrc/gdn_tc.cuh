@@ -780,12 +780,13 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
       const float *cs = reinterpret_cast<const float *>(sg + CS::c);
       // v of channel (row) rr of node n, window element j weighted by wsl[j]
+      // (element 0 is the node's own input row, never a cached row)
       auto vconv = [&](int n, int rr, const float (&wsl)[LBX_MAX_CONV_WIDTH]) {
         const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * n);
         const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
-        float y = 0.f;
+        float y = wsl[0] * bf2f(xs[wj[0] * kTcD + rr]);
 #pragma unroll
-        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
+        for (int j = 1; j < LBX_MAX_CONV_WIDTH; ++j) {
           const int w = wj[j];
           const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + rr]);
           const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + rr];
