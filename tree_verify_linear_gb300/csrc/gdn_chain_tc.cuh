@@ -518,17 +518,29 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 #pragma unroll
         for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
           wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
+        if (t0 >= LBX_MAX_CONV_WIDTH - 1) {
+          // past the first chunk every window row is a staged input row
 #pragma unroll
-        for (int i = 0; i < NH; ++i) {
-          float y = 0.f;
+          for (int i = 0; i < NH; ++i) {
+            float y = 0.f;
 #pragma unroll
-          for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
-            const int w = chain_win(t0, n0 + i, j, K);
-            const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
-            const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
-            y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
+            for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
+              y = fmaf(wslot[j], bf2f(xs[chain_win(t0, n0 + i, j, K) * kTcD + r]), y);
+            vv[i] = silu_fast(y);
           }
-          vv[i] = silu_fast(y);
+        } else {
+#pragma unroll
+          for (int i = 0; i < NH; ++i) {
+            float y = 0.f;
+#pragma unroll
+            for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j) {
+              const int w = chain_win(t0, n0 + i, j, K);
+              const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
+              const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
+              y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
+            }
+            vv[i] = silu_fast(y);
+          }
         }
       }
       ptx::named_sync(1, kTcThreads);  // v inputs consumed
