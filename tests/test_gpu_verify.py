@@ -273,6 +273,14 @@ TC_EDGE = {
     "n64_ddtree_b4": tc(N=64, max_children=4, seed=1122),
     "n64_three_requests": tc(Bq=3, N=64, max_children=4, seed=1123),
     "n48_k2_g4": tc(N=48, K=2, Hk=1, Hv=4, tree="uniform", seed=1124),
+    # node capacities 32 and 64 (16-warp step, prep with the new conv window
+    # kept aside during the conv) at the other conv widths and with the
+    # accepted node at the root (the new window is old cached rows + root)
+    "n64_k3": tc(N=64, K=3, max_children=4, seed=1125),
+    "n30_k1_g1": tc(N=30, K=1, Hk=3, Hv=3, seed=1126),
+    "n64_root": tc(N=64, accepted="root", seed=1127),
+    "n22_root": tc(N=22, accepted="root", seed=1128),
+    "n40_k2_root": tc(N=40, K=2, accepted="root", seed=1129),
 }
 
 

@@ -21,7 +21,8 @@ tiny / serving / long-chain variants of the same layer shapes:
   parent[i] drawn over nodes j < i with weight 2^-depth(j), restricted to
   depth(j) <= 8 (root-to-node paths of at most 10 nodes), optionally with at
   most ``max_children`` children per node.  "chain": parent[i] = i - 1.
-* accepted node: "leaf" (random leaf), "node" (uniform random node), "last".
+* accepted node: "leaf" (random leaf), "node" (uniform random node), "last",
+  "root".
 * slots: request b uses cache slot ``slot[b]``; the pool has ``spare_slots``
   extra slots that no request names, filled with a canary byte pattern.
 
@@ -52,7 +53,7 @@ class Workload:
     d: int            # d_k = d_v
     K: int = 4        # conv width
     tree: str = "ddtree"          # uniform | ddtree | chain
-    accepted: str = "node"        # leaf | node | last
+    accepted: str = "node"        # leaf | node | last | root
     max_children: Optional[int] = None
     max_parent_depth: int = 8
     spare_slots: int = 2
@@ -143,6 +144,8 @@ def pick_accepted(rng: np.random.Generator, parent: np.ndarray, kind: str) -> in
     N = parent.shape[0]
     if kind == "last":
         return N - 1
+    if kind == "root":
+        return 0
     if kind == "node":
         return int(rng.integers(0, N))
     if kind == "leaf":
