@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       ptx::mma_commit(mma_bar);
     }
 
-    // ================= v of this row for this half's nodes (staged inputs) =================
+    // ================= v of this row for this part's nodes (staged inputs) =================
     // The lead warp (warp 0) has just issued MMA1, so it computes only its
     // first NQ - kVOff nodes; warps 1..kVOff each compute one of its other
     // nodes for its 32 rows and pass the values through shared memory.
@@ -839,16 +839,16 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
     float oq[NQ];
-    auto rhs_half = [&](auto hfc) {
-      constexpr int HF = decltype(hfc)::value;
+    auto rhs_part = [&](auto pc) {
+      constexpr int HF = decltype(pc)::value;
       constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
       constexpr int NL = round_up(SH + NQ, LB);
       // rhs_n = b_n v_n - b_n a_n gamma_p S0 k_n (0 for padding nodes)
       float rhs[NQ];
       // accumulator columns in pieces of CH * LB (all at once for small
-      // halves; 8 columns at a time for the large ones, to bound registers)
+      // parts; 8 columns at a time for the large ones, to bound registers)
       constexpr int CH = NQ > 12 ? 1 : NL / LB;
-      static_assert(CH == NL / LB || SH == 0, "chunked halves start aligned");
+      static_assert(CH == NL / LB || SH == 0, "chunked parts start aligned");
 #pragma unroll
       for (int c0 = 0; c0 < NL / LB; c0 += CH) {
         float k_hi[CH * LB], k_lo[CH * LB], q_hi[CH * LB], q_lo[CH * LB];
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, rhs);
     };
-    by_part<PARTS>(pt, rhs_half);
+    by_part<PARTS>(pt, rhs_part);
     // gamma_acc S0 into the MMA3 accumulator (the S0 columns, free since
     // MMA1 completed), this thread's columns; the stage is not read again
 #pragma unroll
@@ -922,8 +922,8 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     // ================= o, path deltas -> tensor memory =================
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
-    auto od_half = [&](auto hfc) {
-      constexpr int HF = decltype(hfc)::value;
+    auto od_part = [&](auto pc) {
+      constexpr int HF = decltype(pc)::value;
       constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
       constexpr int NL = round_up(SH + NQ, LB);
       constexpr int CH = NQ > 12 ? 1 : NL / LB;
@@ -951,7 +951,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, dl);
     };
-    by_part<PARTS>(pt, od_half);
+    by_part<PARTS>(pt, od_part);
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     if (__syncthreads_or(bad)) {  // ---------------------------------------------- S3
