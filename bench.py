@@ -57,6 +57,15 @@ def step_kernels(w):
     return ("gdn_step_kernel",)
 
 
+def step_dtype(w) -> str:
+    """Arithmetic of the path the step runs: the tensor-core kernels take
+    their products as three bf16 passes (hi*hi + hi*lo + lo*hi) with fp32
+    accumulation, the CUDA-core kernel plain fp32."""
+    if w.d == 128:
+        return "f32 (tensor-core products as 3-pass bf16 hi/lo splits, fp32 accumulate)"
+    return "f32"
+
+
 def algorithmic_bytes(w) -> int:
     """Bytes one fused step must move at minimum: state and conv window read
     and written once per (layer, request), conv weights once per layer, the
@@ -377,7 +386,8 @@ def run_lbx(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": step_dtype(w),
         "data": "synthetic",
         "config": {"workload": describe(w), "L": w.L, "Bq": w.Bq, "N": w.N, "Hk": w.Hk,
                    "Hv": w.Hv, "d": w.d, "K": w.K, "parallelism": f"replicas x{world}",

@@ -188,7 +188,8 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
  * device memory -- for instance an engine that reserves all device memory
  * for its caches up front and allows no later cudaMalloc (which would also
  * synchronise the device), or a plugin inside a host framework that owns the
- * only allocator.  The paper has no counterpart to this entry point.
+ * only allocator.  The paper (the Lucebox hub README) has no counterpart to
+ * this entry point.
  *
  * Arguments and results are those of lbx_verify_step minus the workspace.
  * The arrival counters live in a fixed device array inside the library
@@ -201,8 +202,12 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
  * The function allocates nothing: no cudaMalloc, cudaFree or other
  * allocating call.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and may be the moment
+ *     the library's kernels and the array are loaded onto that device; make
+ *     that first call during set-up, before any stream capture.  The address
+ *     is kept for the life of the process: it does not survive
+ *     cudaDeviceReset (or any other teardown of the device's primary
+ *     context), after which this entry point must not be called again.
  *   - Each call clears the counters it uses (cudaMemsetAsync on `stream`)
  *     before launching, since the array keeps the previous call's contents.
  *   - All calls on a device share the one array: calls that overlap on the

@@ -27,7 +27,7 @@
  *      path ending at the accepted node (continuing into the old cache) are
  *      written back to the request's slot.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *   - value head h reads key head h / (Hv/Hk) (contiguous GQA groups);
  *   - conv channels are ordered q | k | v, conv has no bias, tap K-1
  *     multiplies the current node;

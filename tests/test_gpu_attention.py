@@ -77,28 +77,30 @@ def test_tiny_all_outputs():
     assert e <= ATTN_TOL, e
 
 
-def test_attn27b_full_size_sampled_layers():
-    """The 16-layer budget-22 workload (the bench's), layers 0 and 15 checked."""
+def test_attn27b_full_size_all_layers():
+    """The 16-layer budget-22 workload (the bench's), every layer checked."""
     w = ATTN_WORKLOADS["attn27b"]
     inp = make_attn_inputs(w)
     o, status, _ = run_attn(w, inp)
     assert status == 0
     assert np.isfinite(o).all()
-    for l in (0, 15):
-        e = err(o[l:l + 1], ref_layers(w, inp, slice(l, l + 1)))
-        assert e <= ATTN_TOL, (l, e)
+    e = err(o, ref_layers(w, inp, slice(0, w.L)))
+    assert e <= ATTN_TOL, e
 
 
 def test_attn27b_serve_ragged_contexts():
-    """Five requests with contexts of 4096..8192 keys and one empty context."""
+    """Five requests with contexts of 4096..8192 keys and one empty context;
+    the first, a middle and the last layer checked (about 9 s of oracle time
+    per layer)."""
     w = ATTN_WORKLOADS["attn27b_serve"]
     inp = make_attn_inputs(w)
     assert inp["ctx_len"][1] == 0
     o, status, _ = run_attn(w, inp)
     assert status == 0
-    l = 7
-    e = err(o[l:l + 1], ref_layers(w, inp, slice(l, l + 1)))
-    assert e <= ATTN_TOL, e
+    assert np.isfinite(o).all()
+    for l in (0, 7, w.L - 1):
+        e = err(o[l:l + 1], ref_layers(w, inp, slice(l, l + 1)))
+        assert e <= ATTN_TOL, (l, e)
 
 
 def small(**kw):
