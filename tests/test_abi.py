@@ -39,6 +39,26 @@ def test_binding_covers_every_declared_symbol():
     assert sorted(lbx.EXPORTS) == declared_functions()
 
 
+def declared_arity():
+    """Parameter count of every function include/*.h declares."""
+    arity = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for name, params in re.findall(r"\b(lbx_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+            params = params.strip()
+            arity[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return arity
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    """Each ctypes prototype the binding sets has as many arguments as the C
+    declaration (a mismatch would shift every argument after it)."""
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, n in arity.items():
+        assert len(getattr(lib, name).argtypes) == n, (name, len(getattr(lib, name).argtypes), n)
+
+
 def test_strerror_and_workspace(lib):
     from tree_verify_linear_gb300 import lbx
     assert lbx.strerror(0) == "ok"
@@ -67,7 +87,7 @@ def test_null_pointers_and_limits_rejected_on_host(lib):
         lbx.LBX_EINVAL
     assert lib.lbx_tree_conv(ctypes.byref(cfg), *([None] * 8)) == lbx.LBX_EINVAL
     assert lib.lbx_tree_deltanet(ctypes.byref(cfg), *([None] * 10)) == lbx.LBX_EINVAL
-    assert lib.lbx_tree_persist(ctypes.byref(cfg), *([None] * 10)) == lbx.LBX_EINVAL
+    assert lib.lbx_tree_persist(ctypes.byref(cfg), *([None] * 9)) == lbx.LBX_EINVAL
     big = lbx.make_cfg(1, 1, lbx.LBX_MAX_TREE_NODES + 1, 2, 4, 32, 4, 1, mode=lbx.LBX_MODE_TREE)
     fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: rejected first
     args = [fake] * 10

@@ -68,7 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.lbx_tree_deltanet.restype = i32
         lib.lbx_tree_deltanet.argtypes = [vp] * 11
         lib.lbx_tree_persist.restype = i32
-        lib.lbx_tree_persist.argtypes = [vp] * 11
+        lib.lbx_tree_persist.argtypes = [vp] * 10
         lib.lbx_verify_step.restype = i32
         lib.lbx_verify_step.argtypes = [vp] * 11 + [vp, ctypes.c_size_t, vp, vp]
         lib.lbx_verify_step_noalloc.restype = i32
