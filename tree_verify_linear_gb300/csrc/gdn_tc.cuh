@@ -19,8 +19,10 @@
 // (root = 0, ..., accepted node = P-1) and the rest follow in index order;
 // parents still precede children.  Thread 0 also issues the bulk-async copies
 // of the state slab S0 (TMA, four 32-column boxes, 128-byte swizzle) into the
-// stage and of the raw inputs, cached window rows and conv weights of the
-// value head's 128 channels into the staging buffer, one tile ahead.
+// stage, as soon as the previous tile's state store has read it, and of the
+// raw inputs, cached window rows and conv weights of the value head's 128
+// channels into the staging buffer, one tile ahead.  A tile computes its v
+// conv first, while its slab is still on the way.
 //
 // With the factored delta rule S_n = gamma_n S0 + sum_{j in path(n)}
 // g(j->n) delta_j k_j^T (g = product of the gates strictly after j), every
@@ -34,8 +36,9 @@
 //   MMA2  [delta_n | (W rhs)_n]  = rhs [T | W]^T     (A = rhs in TMEM, K = N)
 //   MMA3  sum_j c_j delta_j k_j^T = (c . delta) K     (A = path deltas, K = P,
 //         B = the K rows of the operand read N-major)
-// and the accepted state gamma_acc S0 + MMA3 is written straight to global
-// memory.  T and W (shared by the 128 rows) are built by one lane per
+// and the accepted state gamma_acc S0 + MMA3 is formed in place over the
+// staged S0 (exact fp32 S0, the MMA3 accumulator from tensor memory) and
+// written back by TMA stores of the four boxes.  T and W (shared by the 128 rows) are built by one lane per
 // (node, ancestor-or-self) pair, each walking its stretch of the parent path,
 // with no barriers.  Loops over nodes are unrolled to the node capacity NMAX
 // and run without run-time guards: padding nodes carry zero gates, taps
@@ -168,7 +171,7 @@ struct TcLayout {
   // TMEM columns: S0 hi | lo; the two halves of [S0 k | S0 q] (hi-row and
   // lo-row products); rhs or path deltas (hi | lo).  [delta | W rhs] reuses
   // the first half of the MMA1 accumulator, the MMA3 accumulator the S0
-  // columns.
+  // columns (free once MMA1 has completed).
   static constexpr uint32_t cA1 = 0, cD1 = 128, cA2 = cD1 + R1, cD2 = cD1;
   static_assert(cA2 + KP <= TcRes<NMAX>::tmem_cols, "tensor memory");
   // byte distance from a T entry of [T|W] to the W entry of the same lane
@@ -181,12 +184,7 @@ struct TcLayout {
   static constexpr int stg = round_up(b2lo + kB2, 128);  // value-head conv inputs
   static constexpr int tb = stg + CS::bytes;           // tree tables
   static constexpr int hr = tb + TabLayout<NMAX>::bytes;  // value-head record
-  // v values of the lead warp's rows for its last kVOff nodes, computed by
-  // warps 1..kVOff (float [kVOff][32])
-  static constexpr int kVOff =
-      NMAX / TcRes<NMAX>::parts / 2 < 7 ? NMAX / TcRes<NMAX>::parts / 2 : 7;
-  static constexpr int vx = hr + HeadLayout<NMAX>::bytes;
-  static constexpr int misc = vx + kVOff * 128;  // ints, see kernel
+  static constexpr int misc = hr + HeadLayout<NMAX>::bytes;  // ints, see kernel
   static constexpr int bars = (misc + 64 + 7) & ~7;   // 6 x uint64
   static constexpr int total = bars + 6 * 8;
   static constexpr int smem_bytes = total;
@@ -631,7 +629,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
   };
   // the key head's [K|Q] image, the request's tree tables and the tile's
   // value-head record, from the workspace the prep kernel filled
-  int n_rec_loads = 0, n_tab_loads = 0, n_hr_loads = 0;
+  int n_rec_loads = 0, n_tab_loads = 0, n_hr_loads = 0, n_stores = 0;
   const unsigned char *imgs = T.ws + tc_tab_bytes<NMAX>(Bq);
   const unsigned char *heads = T.ws + tc_head_offset<NMAX>(A.L, Bq, Hk);
   auto load_rec = [&](const Tile &x) {
@@ -729,28 +727,70 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     }
     ptx::fence_proxy_async();
 
+    // ================= v of this row for this part's nodes (staged inputs) =================
+    // before the slab is needed: the v conv covers the slab copy's latency
+    wait_on(stg_bar, stg_waits);
+    float vv[NQ];
+    {
+      const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
+      const float *cs = reinterpret_cast<const float *>(sg + CS::c);
+      float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
+      {
+        const uint16_t *ws = reinterpret_cast<const uint16_t *>(sg + CS::w) + r * K;
+#pragma unroll
+        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
+          wslot[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
+      }
+      // v of this row for node n0 + i, window element j weighted by wslot[j]
+      // (element 0 is the node's own input row, never a cached row)
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * (n0 + i));
+        const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
+        float y = wslot[0] * bf2f(xs[wj[0] * kTcD + r]);
+#pragma unroll
+        for (int j = 1; j < LBX_MAX_CONV_WIDTH; ++j) {
+          const int w = wj[j];
+          const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + r]);
+          const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + r];
+          y = fmaf(wslot[j], w >= 0 ? xn : xc, y);
+        }
+        vv[i] = silu_fast(y);
+      }
+      // this row's value channel of the conv window (only this tile reads it)
+      if (pt == 0) {
+#pragma unroll
+        for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
+          if (rr < K - 1) {
+            const int w = crow[rr];
+            const float v = w >= 0 ? bf2f(xs[w * kTcD + r]) : cs[(-1 - w) * kTcD + r];
+            cache_o[(size_t)rr * C + (2 * Hk + h) * kTcD + r] = v;
+          }
+      }
+    }
+    ptx::named_sync(1, NT);  // staging consumed
+    if (lead && it + 1 < count) load_block(nx);
+
     // ================= S0 -> tensor memory (bf16 hi / lo) =================
     if (!ptx::mbar_wait(stage_bar, (uint32_t)(it & 1))) {
       if (A.status) *A.status = LBX_ETIMEOUT;
       bad = true;
     }
     {
-      // this thread's CPP columns of the row: hi into A columns pt * CPP / 2
-      // .., lo 64 columns further
-      uint32_t vh[CPP / 2], vl[CPP / 2];
+      // this thread's CPP columns of the row, 32 at a time: hi into A
+      // columns pt * CPP / 2 .., lo 64 columns further
 #pragma unroll
-      for (int q = 0; q < CPP / 4; ++q) {
-        const float4 x4 =
-            *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, pt * CPP + 4 * q));
-        split_bf16x2(x4.x, x4.y, vh[2 * q], vl[2 * q]);
-        split_bf16x2(x4.z, x4.w, vh[2 * q + 1], vl[2 * q + 1]);
-      }
-      if constexpr (CPP == 64) {
-        ptx::tmem_st32(tq + Ly::cA1 + pt * 32, vh);
-        ptx::tmem_st32(tq + Ly::cA1 + 64 + pt * 32, vl);
-      } else {
-        ptx::tmem_st16(tq + Ly::cA1 + pt * 16, vh);
-        ptx::tmem_st16(tq + Ly::cA1 + 64 + pt * 16, vl);
+      for (int c = 0; c < CPP / 32; ++c) {
+        uint32_t vh[16], vl[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x4 =
+              *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, pt * CPP + 32 * c + 4 * q));
+          split_bf16x2(x4.x, x4.y, vh[2 * q], vl[2 * q]);
+          split_bf16x2(x4.z, x4.w, vh[2 * q + 1], vl[2 * q + 1]);
+        }
+        ptx::tmem_st16(tq + Ly::cA1 + pt * (CPP / 2) + 16 * c, vh);
+        ptx::tmem_st16(tq + Ly::cA1 + 64 + pt * (CPP / 2) + 16 * c, vl);
       }
     }
     ptx::tmem_wait_st();
@@ -767,71 +807,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       ptx::mma_commit(mma_bar);
     }
 
-    // ================= v of this row for this part's nodes (staged inputs) =================
-    // The lead warp (warp 0) has just issued MMA1, so it computes only its
-    // first NQ - kVOff nodes; warps 1..kVOff each compute one of its other
-    // nodes for its 32 rows and pass the values through shared memory.
-    wait_on(stg_bar, stg_waits);
-    float vv[NQ];
-    constexpr int kVOff = Ly::kVOff, kVOwn = NQ - kVOff;
-    static_assert(kVOwn > 0 && kVOff < NT / 32, "v conv offload");
-    float *vx = reinterpret_cast<float *>(smem + Ly::vx);
-    {
-      const uint16_t *xs = reinterpret_cast<const uint16_t *>(sg + CS::x);
-      const float *cs = reinterpret_cast<const float *>(sg + CS::c);
-      // v of channel (row) rr of node n, window element j weighted by wsl[j]
-      // (element 0 is the node's own input row, never a cached row)
-      auto vconv = [&](int n, int rr, const float (&wsl)[LBX_MAX_CONV_WIDTH]) {
-        const int4 w4 = *reinterpret_cast<const int4 *>(win + 4 * n);
-        const int wj[4] = {w4.x, w4.y, w4.z, w4.w};
-        float y = wsl[0] * bf2f(xs[wj[0] * kTcD + rr]);
-#pragma unroll
-        for (int j = 1; j < LBX_MAX_CONV_WIDTH; ++j) {
-          const int w = wj[j];
-          const float xn = bf2f(xs[(w >= 0 ? w : 0) * kTcD + rr]);
-          const float xc = cs[(w >= 0 ? 0 : -1 - w) * kTcD + rr];
-          y = fmaf(wsl[j], w >= 0 ? xn : xc, y);
-        }
-        return silu_fast(y);
-      };
-      auto weights = [&](int rr, float (&wsl)[LBX_MAX_CONV_WIDTH]) {
-        const uint16_t *ws = reinterpret_cast<const uint16_t *>(sg + CS::w) + rr * K;
-#pragma unroll
-        for (int j = 0; j < LBX_MAX_CONV_WIDTH; ++j)
-          wsl[j] = j < K ? bf2f(ws[K - 1 - j >= 0 ? K - 1 - j : 0]) : 0.f;
-      };
-      float wslot[LBX_MAX_CONV_WIDTH];  // weight of window element j
-      weights(r, wslot);
-      if (warp == 0) {
-#pragma unroll
-        for (int i = 0; i < kVOwn; ++i) vv[i] = vconv(n0 + i, r, wslot);
-      } else {
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) vv[i] = vconv(n0 + i, r, wslot);
-        if (warp <= kVOff) {
-          const int lane = tid & 31;
-          float w0[LBX_MAX_CONV_WIDTH];
-          weights(lane, w0);
-          vx[(warp - 1) * 32 + lane] = vconv(kVOwn + warp - 1, lane, w0);
-        }
-      }
-      // this row's value channel of the conv window (only this tile reads it)
-      if (pt == 0) {
-#pragma unroll
-        for (int rr = 0; rr < LBX_MAX_CONV_WIDTH - 1; ++rr)
-          if (rr < K - 1) {
-            const int w = crow[rr];
-            const float v = w >= 0 ? bf2f(xs[w * kTcD + r]) : cs[(-1 - w) * kTcD + r];
-            cache_o[(size_t)rr * C + (2 * Hk + h) * kTcD + r] = v;
-          }
-      }
-    }
-    ptx::named_sync(1, NT);  // staging consumed
-    if (lead && it + 1 < count) load_block(nx);
-    if (warp == 0) {
-#pragma unroll
-      for (int i = kVOwn; i < NQ; ++i) vv[i] = vx[(i - kVOwn) * 32 + (tid & 31)];
-    }
 
     // ================= rhs -> tensor memory =================
     // Accumulator columns are read in aligned blocks of LB covering this
@@ -875,22 +850,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       store_pairs<NMAX, HF>(tq + Ly::cA2, rhs);
     };
     by_part<PARTS>(pt, rhs_part);
-    // gamma_acc S0 into the MMA3 accumulator (the S0 columns, free since
-    // MMA1 completed), this thread's columns; the stage is not read again
-#pragma unroll
-    for (int c = 0; c < CPP / 32; ++c) {
-      const int k0 = CPP * pt + 32 * c;
-      uint32_t gs[32];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 s4 = *reinterpret_cast<const float4 *>(st + sw128_f32(kTcD, r, k0 + 4 * q));
-        gs[4 * q] = __float_as_uint(gacc * s4.x);
-        gs[4 * q + 1] = __float_as_uint(gacc * s4.y);
-        gs[4 * q + 2] = __float_as_uint(gacc * s4.z);
-        gs[4 * q + 3] = __float_as_uint(gacc * s4.w);
-      }
-      ptx::tmem_st32(tq + Ly::cA1 + k0, gs);
-    }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     if (__syncthreads_or(bad)) {  // ---------------------------------------------- S2
@@ -916,7 +875,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
         }
       }
       ptx::mma_commit(mma_bar);
-      if (it + 1 < count) load_state(nx);  // the stage has been read
     }
 
     // ================= o, path deltas -> tensor memory =================
@@ -964,7 +922,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kTcD);
       const uint32_t b1_a = ptx::smem_u32(B1);
-      uint32_t accum = 1;  // onto gamma_acc S0
+      uint32_t accum = 0;
 #pragma unroll 1
       for (int pass = 0; pass < 3; ++pass) {
         const uint32_t a_col = Ly::cA2 + (pass == 2 ? KH : 0);
@@ -988,31 +946,45 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       if (ptx::mbar_wait(mma_bar, mma_waits & 1u)) load_rec(nx);
     }
 
-    // ================= accepted state row (gamma_acc S0 + MMA3) -> global memory =================
+    // ================= accepted state (gamma_acc S0 + MMA3) -> global memory =================
+    // formed in place over this thread's bytes of the staged S0 (the box
+    // layout the copies use), then stored by TMA; the next slab follows
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
     {
-      float *srow =
-          A.state_out + ((((size_t)l * A.n_slots + slot_b) * Hv + h) * kTcD + r) * kTcD;
-      // this thread's columns, 32 at a time
+      const int sw = r & 7;
 #pragma unroll
       for (int c = 0; c < CPP / 32; ++c) {
-        const int k0 = CPP * pt + 32 * c;
+        const int box = (CPP * pt) / 32 + c;
+        unsigned char *row = st + box * (kStageBytes / 4) + r * 128;
         float d[32];
-        ptx::tmem_ld32(tq + Ly::cA1 + k0, d);
+        ptx::tmem_ld32(tq + Ly::cA1 + 32 * box, d);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          stg_v8(srow + k0 + 8 * q, d[8 * q], d[8 * q + 1], d[8 * q + 2], d[8 * q + 3],
-                 d[8 * q + 4], d[8 * q + 5], d[8 * q + 6], d[8 * q + 7]);
+        for (int q = 0; q < 8; ++q) {
+          float4 *p4 = reinterpret_cast<float4 *>(row + ((q ^ sw) << 4));
+          const float4 s4 = *p4;
+          *p4 = make_float4(fmaf(gacc, s4.x, d[4 * q]), fmaf(gacc, s4.y, d[4 * q + 1]),
+                            fmaf(gacc, s4.z, d[4 * q + 2]), fmaf(gacc, s4.w, d[4 * q + 3]));
+        }
       }
     }
+    ptx::fence_proxy_async();  // the staged rows, for the TMA stores
     ptx::tc_fence_before();
     if (__syncthreads_or(bad)) {  // ---------------------------------------------- S4
       aborted = true;
       break;
     }
-    if (lead && it + 1 < count && nx.bq != bq) load_tab(nx);
+    if (lead) {
+      const int srow = ((l * A.n_slots + slot_b) * Hv + h) * kTcD;
+      for (int a = 0; a < 4; ++a)
+        ptx::tma_store_2d(&maps.state, a * 32, srow, st + a * (kStageBytes / 4));
+      ptx::bulk_commit();
+      ++n_stores;
+      ptx::bulk_wait_read_all();  // the stage may be refilled
+      if (it + 1 < count) load_state(nx);
+      if (it + 1 < count && nx.bq != bq) load_tab(nx);
+    }
   }
 
   // ---- drain: copies still in flight after an abort ----
@@ -1023,6 +995,8 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     if (n_tab_loads > 0) (void)ptx::mbar_wait(tab_bar, (uint32_t)((n_tab_loads - 1) & 1));
     if (n_hr_loads > 0) (void)ptx::mbar_wait(hr_bar, (uint32_t)((n_hr_loads - 1) & 1));
   }
+  // the state stores complete before the CTA leaves
+  if (lead && n_stores > 0) ptx::bulk_wait_all();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
