@@ -710,6 +710,10 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
 
     // ================= [T | W] of this value head =================
     wait_on(hr_bar, hr_waits);
+    if (lead && it > 0) {
+      ptx::bulk_wait_read_all();  // the previous tile's stores have read the stage
+      load_state(x);
+    }
     ptx::named_sync(1, NT);  // zero-filled [T|W] (new request) before the scatter
     const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
     {
@@ -981,8 +985,9 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
         ptx::tma_store_2d(&maps.state, a * 32, srow, st + a * (kStageBytes / 4));
       ptx::bulk_commit();
       ++n_stores;
-      ptx::bulk_wait_read_all();  // the stage may be refilled
-      if (it + 1 < count) load_state(nx);
+      // the next slab is loaded once the stores have read the stage: after
+      // the next tile's record wait, so that the issuing thread does not
+      // stall here while the stores drain
       if (it + 1 < count && nx.bq != bq) load_tab(nx);
     }
   }
