@@ -140,23 +140,27 @@ struct GramLayout {
   static_assert(bytes % 16 == 0, "alignment");
 };
 
-// Per-value-head record (built by the prep kernel, bulk-copied per tile):
-// the T and W entries of every (node, ancestor-or-self) lane, and in the new
-// labels the gates a, b, gamma of the parent (product of the ancestors'
-// gates), the accepted-path coefficients g(j->acc), then gamma of the
-// accepted node.
+// Per-value-head record (built by the prep kernel, bulk-copied per tile): in
+// the new labels the gates a, b, gamma of the parent (product of the
+// ancestors' gates), the accepted-path coefficients g(j->acc), gamma of the
+// accepted node, then the T and the W entries of the tree's (node,
+// ancestor-or-self) lanes.  A record's slot holds every lane a tree of NMAX
+// nodes can have; only used(lanes) bytes of it are written and read.
 template <int NMAX>
 struct HeadLayout {
   static constexpr int kNLaneP = round_up(NMAX * (NMAX + 1) / 2, 4);
   static constexpr int NP = round_up(NMAX, 4);
-  static constexpr int tw = 0;                 // float [2][kNLaneP]: T, then W
-  static constexpr int an = tw + 8 * kNLaneP;  // float [NP]
+  static constexpr int an = 0;                 // float [NP]
   static constexpr int bn = an + 4 * NP;
   static constexpr int gam = bn + 4 * NP;
   static constexpr int cpa = gam + 4 * NP;
   static constexpr int gacc = cpa + 4 * NP;    // float [4]
-  static constexpr int bytes = gacc + 16;
-  static_assert(bytes % 16 == 0, "alignment");
+  static constexpr int tw = gacc + 16;         // float [2][lanes4]: T, then W
+  static constexpr int bytes = tw + 8 * kNLaneP;
+  // lanes rounded up to 4: the W entries start that many floats after T's
+  __host__ __device__ static constexpr int lanes4(int lanes) { return round_up(lanes, 4); }
+  __host__ __device__ static constexpr int used(int lanes) { return tw + 8 * lanes4(lanes); }
+  static_assert(tw % 16 == 0 && bytes % 16 == 0, "alignment");
 };
 
 template <int NMAX>
@@ -637,9 +641,12 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     ptx::bulk_load(B1, imgs + (size_t)x.rest * Ly::kB, (uint32_t)Ly::kB, rec_bar);
     ++n_rec_loads;
   };
-  auto load_hr = [&](int t) {
-    ptx::mbar_arrive_expect_tx(hr_bar, (uint32_t)HL::bytes);
-    ptx::bulk_load(hr, heads + (size_t)t * HL::bytes, (uint32_t)HL::bytes, hr_bar);
+  // the record of tile t: its used bytes when the tile's request is the one
+  // whose tables are in shared memory (their lane count), else all of it
+  auto load_hr = [&](int t, bool tables_match) {
+    const uint32_t n = tables_match ? (uint32_t)HL::used(meta[1]) : (uint32_t)HL::bytes;
+    ptx::mbar_arrive_expect_tx(hr_bar, n);
+    ptx::bulk_load(hr, heads + (size_t)t * HL::bytes, n, hr_bar);
     ++n_hr_loads;
   };
   auto load_tab = [&](const Tile &x) {
@@ -669,7 +676,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     ptx::wait_prerequisite_grid();
     load_tab(cur);
     load_rec(cur);
-    load_hr(t_begin);
+    load_hr(t_begin, false);
   }
 
   // state row r (= TMEM lane) and part pt of this thread; the row work of
@@ -717,12 +724,12 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     ptx::named_sync(1, NT);  // zero-filled [T|W] (new request) before the scatter
     const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
     {
-      const int nl = meta[1];
+      const int nl = meta[1], nl4 = HL::lanes4(nl);
       for (int lane = tid; lane < nl; lane += NT) {
         const uint32_t o = lofs[lane];
         uint16_t th, tl, wh, wl;
         split_bf16(tw[lane], th, tl);
-        split_bf16(tw[HL::kNLaneP + lane], wh, wl);
+        split_bf16(tw[nl4 + lane], wh, wl);
         *reinterpret_cast<uint16_t *>(B2hi + o) = th;
         *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
         *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
@@ -942,7 +949,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       ptx::mma_commit(mma_bar);
       // every thread has passed its last read of this tile's value-head
       // record (S3): bring in the next tile's
-      if (it + 1 < count) load_hr(t + 1);
+      if (it + 1 < count) load_hr(t + 1, nx.bq == bq);
     }
     if (lead && it + 1 < count && nx.rest != x.rest) {
       // the next tile starts a key head: its record replaces this one once

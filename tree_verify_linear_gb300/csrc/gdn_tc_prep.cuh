@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(TcRes<NMAX>::prep_threads, TcRes<NMAX>::prep_c
       float *hrec = reinterpret_cast<float *>(
           heads + ((size_t)lbi * Hv + kh * G + hc + hh) * HL::bytes + HL::tw);
       hrec[lane] = xl;
-      hrec[HL::kNLaneP + lane] = fmaf(kqn[n], xl, an[n] * s);
+      hrec[HL::lanes4(nl) + lane] = fmaf(kqn[n], xl, an[n] * s);
       if (L == dep[n]) hgam[hh * NP + n] = gp;  // product of the gates of all ancestors
     }
     __syncthreads();
