@@ -63,7 +63,9 @@ extern "C" {
 
 /* Limits. */
 #define LBX_MAX_TREE_NODES 64 /* tree mode: N <= 64 nodes per request          */
-#define LBX_CHAIN_CHUNK 64    /* chunked (chain) mode processes 64 tokens/chunk */
+#define LBX_CHAIN_CHUNK 64    /* chunked mode, CUDA-core path (d != 128): tokens
+                                 per chunk; the d = 128 tensor-core chain kernel
+                                 walks the chain 16 tokens at a time           */
 #define LBX_MAX_CONV_WIDTH 4  /* 1 <= K <= 4                                    */
 #define LBX_ACCEPT_MAX_NODES 4096 /* lbx_accept_walk: N <= 4096 nodes         */
 #define LBX_DDTREE_MAX_K 8        /* lbx_ddtree_build: top-K, 1 <= K <= 8       */
@@ -169,9 +171,13 @@ int lbx_tree_persist(const lbx_cfg *cfg, const uint16_t *x, const float *node_st
  *   state [L][n_slots][Hv][d][d], conv_cache [L][n_slots][K-1][C]  fp32, in/out
  *   o [L][Bq][N][Hv][d]                                     fp32, out
  *   workspace / workspace_bytes: >= lbx_workspace_size(cfg) bytes (see there)
- * Modes: in tree mode N <= LBX_MAX_TREE_NODES; chunked mode takes a chain of
- * any length and processes it LBX_CHAIN_CHUNK tokens at a time.  Distinct
- * requests must name distinct slots.
+ * Modes: in tree mode N <= LBX_MAX_TREE_NODES (the tensor-core step keeps node
+ * labels as bytes, two nodes per lane of the warp that builds a request's
+ * tables, and the CUDA-core step's S0 [K|Q] product tile covers at most 2N =
+ * 128 columns at d = 128); chunked mode takes a chain of any length: at d =
+ * 128 on the tensor cores in chunks of 16 tokens, otherwise on CUDA cores in
+ * chunks of LBX_CHAIN_CHUNK tokens.  Distinct requests must name distinct
+ * slots.
  */
 int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_w,
                     const uint16_t *a, const uint16_t *b, const int32_t *parent,
