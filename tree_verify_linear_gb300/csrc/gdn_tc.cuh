@@ -19,9 +19,10 @@
 // (root = 0, ..., accepted node = P-1) and the rest follow in index order;
 // parents still precede children.  Thread 0 also issues the bulk-async copies
 // of the state slab S0 (TMA, four 32-column boxes, 128-byte swizzle) into the
-// stage, as soon as the previous tile's state store has read it, and of the
-// raw inputs, cached window rows and conv weights of the value head's 128
-// channels into the staging buffer, one tile ahead.  A tile computes its v
+// stage, as soon as the previous tile's state store has read it (at two CTAs
+// per SM the next tile's slab is first prefetched into L2 a tile ahead), and
+// of the raw inputs, cached window rows and conv weights of the value head's
+// 128 channels into the staging buffer, one tile ahead.  A tile computes its v
 // conv first, while its slab is still on the way.
 //
 // With the factored delta rule S_n = gamma_n S0 + sum_{j in path(n)}
@@ -720,6 +721,13 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
     if (lead && it > 0) {
       ptx::bulk_wait_read_all();  // the previous tile's stores have read the stage
       load_state(x);
+    }
+    if (TcRes<NMAX>::ctas == 2 && lead && it + 1 < count) {
+      // the next tile's slab into L2 while this tile runs, so that its copy
+      // into the stage at the next tile's top reads L2 (at one CTA per SM,
+      // 32 nodes and more, this measured slower and is left out)
+      const int srow = ((nx.l * A.n_slots + slot_of(lead_slots, nx.bq)) * Hv + nx.h) * kTcD;
+      ptx::prefetch_l2(A.state_in + (size_t)srow * kTcD, kStageBytes, ptx::policy_evict_last());
     }
     ptx::named_sync(1, NT);  // zero-filled [T|W] (new request) before the scatter
     const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];

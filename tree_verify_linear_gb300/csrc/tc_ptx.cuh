@@ -85,6 +85,19 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int 
                "r"(x), "r"(y), "r"(smem_u32(src))
                : "memory");
 }
+// L2 cache policy that keeps lines ahead of others (data read again soon).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Bulk prefetch of global memory into L2 (nothing to wait for); address
+// 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(pol)
+               : "memory");
+}
 // Plain (non-tensor) bulk copy global -> shared, completing on `bar`; both
 // addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
