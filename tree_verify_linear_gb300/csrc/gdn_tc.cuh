@@ -23,7 +23,8 @@
 // per SM the next tile's slab is first prefetched into L2 a tile ahead), and
 // of the raw inputs, cached window rows and conv weights of the value head's
 // 128 channels into the staging buffer, one tile ahead.  A tile computes its v
-// conv first, while its slab is still on the way.
+// conv first, while its slab and its value-head record are still on the way,
+// and writes o while MMA3 runs.
 //
 // With the factored delta rule S_n = gamma_n S0 + sum_{j in path(n)}
 // g(j->n) delta_j k_j^T (g = product of the gates strictly after j), every
@@ -39,9 +40,9 @@
 //         B = the K rows of the operand read N-major)
 // and the accepted state gamma_acc S0 + MMA3 is formed in place over the
 // staged S0 (exact fp32 S0, the MMA3 accumulator from tensor memory) and
-// written back by TMA stores of the four boxes.  T and W (shared by the 128 rows) are built by one lane per
-// (node, ancestor-or-self) pair, each walking its stretch of the parent path,
-// with no barriers.  Loops over nodes are unrolled to the node capacity NMAX
+// written back by TMA stores of the four boxes.  T and W (shared by the 128
+// rows) are built by one lane per (node, ancestor-or-self) pair, each walking
+// its stretch of the parent path, with no barriers.  Loops over nodes are unrolled to the node capacity NMAX
 // and run without run-time guards: padding nodes carry zero gates, taps
 // beyond the conv width zero weights, every load a clamped, valid index.
 // The conv window of the slot is persisted in place: every value channel by
@@ -716,8 +717,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       wait_on(rec_bar, rec_waits);
     }
 
-    // ================= [T | W] of this value head =================
-    wait_on(hr_bar, hr_waits);
     if (lead && it > 0) {
       ptx::bulk_wait_read_all();  // the previous tile's stores have read the stage
       load_state(x);
@@ -729,22 +728,6 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       const int srow = ((nx.l * A.n_slots + slot_of(lead_slots, nx.bq)) * Hv + nx.h) * kTcD;
       ptx::prefetch_l2(A.state_in + (size_t)srow * kTcD, kStageBytes, ptx::policy_evict_last());
     }
-    ptx::named_sync(1, NT);  // zero-filled [T|W] (new request) before the scatter
-    const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
-    {
-      const int nl = meta[1], nl4 = HL::lanes4(nl);
-      for (int lane = tid; lane < nl; lane += NT) {
-        const uint32_t o = lofs[lane];
-        uint16_t th, tl, wh, wl;
-        split_bf16(tw[lane], th, tl);
-        split_bf16(tw[nl4 + lane], wh, wl);
-        *reinterpret_cast<uint16_t *>(B2hi + o) = th;
-        *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
-        *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
-        *reinterpret_cast<uint16_t *>(B2lo + o + Ly::kWOff) = wl;
-      }
-    }
-    ptx::fence_proxy_async();
 
     // ================= v of this row for this part's nodes (staged inputs) =================
     // before the slab is needed: the v conv covers the slab copy's latency
@@ -787,8 +770,25 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
           }
       }
     }
-    ptx::named_sync(1, NT);  // staging consumed
+    // ================= [T | W] of this value head =================
+    wait_on(hr_bar, hr_waits);
+    ptx::named_sync(1, NT);  // staging consumed; zero-filled [T|W] (new request) before the scatter
     if (lead && it + 1 < count) load_block(nx);
+    const float gacc = reinterpret_cast<const float *>(hr + HL::gacc)[0];
+    {
+      const int nl = meta[1], nl4 = HL::lanes4(nl);
+      for (int lane = tid; lane < nl; lane += NT) {
+        const uint32_t o = lofs[lane];
+        uint16_t th, tl, wh, wl;
+        split_bf16(tw[lane], th, tl);
+        split_bf16(tw[nl4 + lane], wh, wl);
+        *reinterpret_cast<uint16_t *>(B2hi + o) = th;
+        *reinterpret_cast<uint16_t *>(B2lo + o) = tl;
+        *reinterpret_cast<uint16_t *>(B2hi + o + Ly::kWOff) = wh;
+        *reinterpret_cast<uint16_t *>(B2lo + o + Ly::kWOff) = wl;
+      }
+    }
+    ptx::fence_proxy_async();
 
     // ================= S0 -> tensor memory (bf16 hi / lo) =================
     if (!ptx::mbar_wait(stage_bar, (uint32_t)(it & 1))) {
@@ -896,39 +896,31 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       ptx::mma_commit(mma_bar);
     }
 
-    // ================= o, path deltas -> tensor memory =================
+    // ================= path deltas -> tensor memory =================
     wait_on(mma_bar, mma_waits);
     ptx::tc_fence_after();
-    auto od_part = [&](auto pc) {
+    auto dl_part = [&](auto pc) {
       constexpr int HF = decltype(pc)::value;
       constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
       constexpr int NL = round_up(SH + NQ, LB);
       constexpr int CH = NQ > 12 ? 1 : NL / LB;
-      float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
       float dl[NQ];
 #pragma unroll
       for (int c0 = 0; c0 < NL / LB; c0 += CH) {
-        float dd[CH * LB], wr[CH * LB];
+        float dd[CH * LB];
 #pragma unroll
-        for (int b = 0; b < CH; ++b) {
-          const int cb = B0 + (c0 + b) * LB;
-          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + cb, dd + b * LB);
-          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + NMAX + cb, wr + b * LB);
-        }
+        for (int b = 0; b < CH; ++b)
+          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + B0 + (c0 + b) * LB, dd + b * LB);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < CH * LB; ++e) {
           const int i = c0 * LB + e - SH;  // node N0 + i
-          if (i >= 0 && i < NQ) {
-            const int n = N0 + i;
-            if (n < N) __stcs(o_base + (size_t)n2o[n] * Hv * kTcD, oq[i] + wr[e]);
-            dl[i] = cpa[n] * dd[e];
-          }
+          if (i >= 0 && i < NQ) dl[i] = cpa[N0 + i] * dd[e];
         }
       }
       store_pairs<NMAX, HF>(tq + Ly::cA2, dl);
     };
-    by_part<PARTS>(pt, od_part);
+    by_part<PARTS>(pt, dl_part);
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     if (__syncthreads_or(bad)) {  // ---------------------------------------------- S3
@@ -959,6 +951,32 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
       // record (S3): bring in the next tile's
       if (it + 1 < count) load_hr(t + 1, nx.bq == bq);
     }
+
+    // ================= o = diag(a gamma_p) S0 q + W rhs, while MMA3 runs =================
+    // (MMA3 writes the S0 columns; W rhs sits in the MMA2 accumulator)
+    ptx::tc_fence_after();
+    auto o_part = [&](auto pc) {
+      constexpr int HF = decltype(pc)::value;
+      constexpr int N0 = HF * NQ, B0 = N0 / LB * LB, SH = N0 - B0;
+      constexpr int NL = round_up(SH + NQ, LB);
+      constexpr int CH = NQ > 12 ? 1 : NL / LB;
+      float *o_base = A.o + (lb * N) * (size_t)Hv * kTcD + (size_t)h * kTcD + r;
+#pragma unroll
+      for (int c0 = 0; c0 < NL / LB; c0 += CH) {
+        float wr[CH * LB];
+#pragma unroll
+        for (int b = 0; b < CH; ++b)
+          ptx::tmem_ld_w<LB>(tq + Ly::cD2 + NMAX + B0 + (c0 + b) * LB, wr + b * LB);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < CH * LB; ++e) {
+          const int i = c0 * LB + e - SH;  // node N0 + i
+          if (i >= 0 && i < NQ && N0 + i < N)
+            __stcs(o_base + (size_t)n2o[N0 + i] * Hv * kTcD, oq[i] + wr[e]);
+        }
+      }
+    };
+    by_part<PARTS>(pt, o_part);
     if (lead && it + 1 < count && nx.rest != x.rest) {
       // the next tile starts a key head: its record replaces this one once
       // MMA3 (the last reader of the operand) has completed
