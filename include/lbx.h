@@ -194,8 +194,9 @@ int lbx_verify_step(const lbx_cfg *cfg, const uint16_t *x, const uint16_t *conv_
  * device memory -- for instance an engine that reserves all device memory
  * for its caches up front and allows no later cudaMalloc (which would also
  * synchronise the device), or a plugin inside a host framework that owns the
- * only allocator.  The paper (the Lucebox hub README) has no counterpart to
- * this entry point.
+ * only allocator.  It computes exactly what lbx_verify_step computes; the
+ * Lucebox hub README describes no such variant, so it has no passage of its
+ * own to cite.
  *
  * Arguments and results are those of lbx_verify_step minus the workspace.
  * The arrival counters live in a fixed device array inside the library
