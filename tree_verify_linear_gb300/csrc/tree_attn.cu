@@ -27,10 +27,13 @@
 // unnormalised partial (running max m, sum l, O) of every row tile it covers
 // to the workspace; the last of a row tile's CTAs to finish merges them.
 //
-// Per CTA: the Q tile (128 x 256 bf16, 128-byte swizzled, K-major) stays in
-// shared memory; K and V blocks of 32 keys arrive by TMA, four blocks in
-// flight; S (two 32-column buffers), P (two buffers, bf16 hi and lo) and O
-// (256 columns) live in tensor memory.  P is split into bf16 hi + lo and
+// Per CTA: the Q tile (128 rows x 256 bf16) stays in tensor memory, written
+// row by row by the softmax threads at the start of each segment; K and V
+// blocks of 64 keys arrive by TMA (four K and three V blocks in flight); S and
+// P of a block share one of two 64-column TMEM buffers (the softmax threads
+// overwrite S with P after the max exchange), and O takes 256 columns.  The
+// issuing thread computes S = Q K^T with A = Q from tensor memory and O += P V
+// with A = P from tensor memory.  P is split into bf16 hi + lo and
 // multiplies V twice, so the product keeps ~2^-17 of relative precision (Q,
 // K and V are exact bf16 inputs, accumulation is fp32).  The softmax
 // reference point moves only when a block's maximum exceeds it by more than
@@ -56,38 +59,43 @@ namespace attn {
 constexpr int kDh = LBX_ATTN_HEAD_DIM;  // head dimension (256)
 constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
 constexpr int kKB = 64;                 // keys per block
-constexpr int kKStages = 3;             // K blocks in flight (S runs two blocks ahead)
-constexpr int kVStages = 2;             // V blocks in flight
+constexpr int kKStages = 4;             // K blocks in flight
+constexpr int kVStages = 3;             // V blocks in flight
 constexpr int kMaxNodes = LBX_ATTN_MAX_NODES;
 // Largest persistent grid (one CTA per SM; a GPU with more SMs uses this
 // many); the workspace holds one partial per (CTA, row tile) piece, at most
 // kMaxCtas + row tiles of them.
 constexpr int kMaxCtas = 160;
 
-// shared memory: Q tile, K stages, V stages, ancestor masks, ints, mbarriers
-constexpr int kQBytes = (kDh / 64) * kRows * 128;  // 64 KB, atoms of 64 dh columns
+// shared memory: K stages, V stages, ancestor masks, ints, mbarriers (the Q
+// tile lives in tensor memory)
 constexpr int kKVAtom = kKB * 128;                 // one 64-column atom of a block
 constexpr int kKBytes = (kDh / 64) * kKVAtom;      // 32 KB: one K (or V) block
-constexpr int kSmemQ = 0;
-constexpr int kSmemK = kQBytes;
+constexpr int kSmemK = 0;
 constexpr int kSmemV = kSmemK + kKStages * kKBytes;
 constexpr int kSmemAnc = kSmemV + kVStages * kKBytes;      // uint64 [64]
 constexpr int kSmemRed = kSmemAnc + kMaxNodes * 8;        // float [2][128]
 constexpr int kSmemMisc = kSmemRed + 2 * kRows * 4;       // int [16]
-constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [13]
-constexpr int kSmemTotal = kSmemBars + 13 * 8;
+constexpr int kNBars = kKStages + kVStages + 6;           // k, v, s[2], o[2], p[2]
+constexpr int kSmemBars = kSmemMisc + 64;                 // uint64 [kNBars]
+constexpr int kSmemTotal = kSmemBars + kNBars * 8;
 // threads: 8 softmax warps (two threads per row) and one issuing warp
 constexpr int kSoftmaxThreads = 2 * kRows;
 constexpr int kThreads = kSoftmaxThreads + 32;
 static_assert(kSmemTotal <= 227 * 1024, "shared memory");
 static_assert(kSmemK % 1024 == 0 && kSmemV % 1024 == 0 && kKBytes % 1024 == 0,
               "swizzled operands");
-// tensor memory columns
-constexpr uint32_t kColS = 0;    // S: two 64-column buffers
-constexpr uint32_t kColP = 128;  // P: two buffers of 64 columns (32 hi, 32 lo)
-constexpr uint32_t kColO = 256;  // O: 256 columns
+// tensor memory columns: the Q tile (operand A of S = Q K^T: row = lane,
+// bf16 pairs along dh); S and P of block q in buffer q & 1 (the softmax
+// threads read S, meet at the max exchange, then overwrite it with P: bf16 hi
+// in the first 32 columns, lo in the other 32, operand A of O += P V); O
+constexpr uint32_t kColQ = 0;     // 128 columns
+constexpr uint32_t kColSP = 128;  // two 64-column buffers
+constexpr uint32_t kColO = 256;   // 256 columns
 constexpr uint32_t kTmemCols = 512;
-static_assert(kColO + kDh <= kTmemCols && kColP + 2 * kKB <= kColO, "tensor memory");
+static_assert(kColQ + kDh / 2 <= kColSP && kColSP + 2 * kKB <= kColO &&
+                  kColO + kDh <= kTmemCols,
+              "tensor memory");
 
 // Row tiles (host and device compute the same).
 struct Geo {
@@ -176,12 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *misc = reinterpret_cast<int *>(smem + kSmemMisc);  // [0] TMEM base, [1] last CTA
   uint64_t *anc = reinterpret_cast<uint64_t *>(smem + kSmemAnc);
   float *red = reinterpret_cast<float *>(smem + kSmemRed);  // [2][kRows] per-half values
-  uint64_t *k_bar = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [3]
-  uint64_t *v_bar = k_bar + 3;                                        // [2]
-  uint64_t *s_bar = k_bar + 5;                                        // [2]
-  uint64_t *o_bar = k_bar + 7;                                        // [2]
-  uint64_t *s_free = k_bar + 9;   // [2] the softmax threads have read S (256 arrivals)
-  uint64_t *p_full = k_bar + 11;  // [2] the softmax threads have stored P (256 arrivals)
+  uint64_t *k_bar = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [kKStages]
+  uint64_t *v_bar = k_bar + kKStages;                                 // [kVStages]
+  uint64_t *s_bar = v_bar + kVStages;                                 // [2]
+  uint64_t *o_bar = s_bar + 2;                                        // [2]
+  uint64_t *p_full = o_bar + 2;  // [2] the softmax threads have stored P (256 arrivals)
 
   // ---- whole-batch validation (the same verdict in every CTA) ----
   {
@@ -215,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up ----
   if (tid == 0) {
-    for (int i = 0; i < 9; ++i) ptx::mbar_init(k_bar + i, 1);
-    for (int i = 9; i < 13; ++i) ptx::mbar_init(k_bar + i, kSoftmaxThreads);
+    for (int i = 0; i < kNBars - 2; ++i) ptx::mbar_init(k_bar + i, 1);
+    for (int i = kNBars - 2; i < kNBars; ++i) ptx::mbar_init(k_bar + i, kSoftmaxThreads);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -235,9 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool softmax = tid < kSoftmaxThreads;
   const bool issuer = tid == kSoftmaxThreads;
 
-  // descriptors of the Q tile and of stage 0; the others are fixed offsets
-  // (added to the 16-byte address field)
-  const uint64_t qdesc = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemQ));
+  // descriptors of stage 0; the others are fixed offsets (added to the
+  // 16-byte address field)
   const uint64_t kdesc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + kSmemK));
   const uint64_t vdesc0 =
       ptx::sdesc(ptx::smem_u32(smem + kSmemV), (uint32_t)kKVAtom, 1024u, 2u);
@@ -289,22 +295,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       anc[tid] = m;
     }
-    {
+    if (softmax) {
+      // this thread's half of its row's q (zero on padding rows) -> the Q
+      // tile in tensor memory, bf16 pairs along dh
       const uint4 *qg = reinterpret_cast<const uint4 *>(A.q);
-      for (int idx = tid; idx < kRows * (kDh / 8); idx += kThreads) {
-        const int rr = idx / (kDh / 8), c16 = idx % (kDh / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (rr < rows) {
-          const int hl = rr / N, n = rr - hl * N;
-          const int hq = kvh * g.G + h0 + hl;
-          v = qg[(((size_t)lb * N + n) * A.Hq + hq) * (kDh / 8) + c16];
-        }
-        const int atom = c16 >> 3, ch = c16 & 7;
-        *reinterpret_cast<uint4 *>(smem + kSmemQ + atom * (kRows * 128) + rr * 128 +
-                                   ((ch ^ (rr & 7)) << 4)) = v;
+      const bool rv = r < rows;
+      size_t qrow = 0;
+      if (rv) {
+        const int hl = r / N, n = r - hl * N;
+        const int hq = kvh * g.G + h0 + hl;
+        qrow = (((size_t)lb * N + n) * A.Hq + hq) * (kDh / 8) + hf * (kDh / 16);
       }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = rv ? qg[qrow + c * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * e] = v.x;
+          w[4 * e + 1] = v.y;
+          w[4 * e + 2] = v.z;
+          w[4 * e + 3] = v.w;
+        }
+        ptx::tmem_st32(tq + kColQ + (uint32_t)(hf * (kDh / 4) + 32 * c), w);
+      }
+      ptx::tmem_wait_st();
     }
-    ptx::fence_proxy_async();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -342,12 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long q = q0 + i;
       const uint64_t kd = kdesc0 + (uint64_t)(((q % kKStages) * kKBytes) >> 4);
       constexpr uint32_t idesc = ptx::idesc_bf16(128, kKB);
-      const uint32_t d = tmem + kColS + (uint32_t)(q & 1) * kKB;
+      const uint32_t d = tmem + kColSP + (uint32_t)(q & 1) * kKB;
 #pragma unroll
       for (int ks = 0; ks < kDh / 16; ++ks) {
-        const uint64_t ao = (uint64_t)(((ks >> 2) * (kRows * 128) + (ks & 3) * 32) >> 4);
         const uint64_t bo = (uint64_t)(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
-        ptx::mma_bf16_ss(d, qdesc + ao, kd + bo, idesc, ks > 0 ? 1u : 0u);
+        ptx::mma_bf16_ts(d, tmem + kColQ + 8u * ks, kd + bo, idesc, ks > 0 ? 1u : 0u);
       }
       ptx::mma_commit(&s_bar[q & 1]);
       ++n_mma1;
@@ -358,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long q = q0 + i;
       const uint64_t vd = vdesc0 + (uint64_t)(((q % kVStages) * kKBytes) >> 4);
       constexpr uint32_t idesc = ptx::idesc_bf16_bmn(128, kDh);
-      const uint32_t pc = tmem + kColP + (uint32_t)(q & 1) * kKB;
+      const uint32_t pc = tmem + kColSP + (uint32_t)(q & 1) * kKB;
       uint32_t accum = acc ? 1u : 0u;
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass)
@@ -383,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < nb && !bad; ++i) {
         const long long q = q0 + i;
-        // the next block's scores, into the other buffer once the softmax
-        // threads have read it (two blocks ago; earlier segments are done)
+        // the next block's scores, into the other buffer once the product
+        // that read its P (block i - 1; earlier segments are done) is done
         if (i + 1 < nb) {
           if (!ptx::mbar_wait(&k_bar[(q + 1) % kKStages], (uint32_t)(((q + 1) / kKStages) & 1)))
             bad = true;
           if (i >= 1 && !bad &&
-              !ptx::mbar_wait(&s_free[(q + 1) & 1], (uint32_t)(((q - 1) >> 1) & 1)))
+              !ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1)))
             bad = true;
           if (!bad) mma1(i + 1);
         }
@@ -405,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bad) break;
         ptx::tc_fence_after();
         mma2(i, i > 0);
-        // the previous product is done: its V stage takes block i + 1
-        if (i >= 1 && i + 1 < nb) {
+        // the previous product is done: its V stage takes block i - 1 + kVStages
+        if (i >= 1 && i - 1 + kVStages < nb) {
           if (!ptx::mbar_wait(&o_bar[(q - 1) & 1], (uint32_t)(((q - 1) >> 1) & 1))) bad = true;
-          if (!bad) load_v(i + 1);
+          if (!bad) load_v(i - 1 + kVStages);
         }
       }
     } else if (softmax) {
@@ -419,10 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!bad && !ptx::mbar_wait(&s_bar[q & 1], (uint32_t)((q >> 1) & 1))) bad = true;
         ptx::tc_fence_after();
         float sv[kHalfKeys];
-        ptx::tmem_ld32(tq + kColS + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
+        ptx::tmem_ld32(tq + kColSP + (uint32_t)(q & 1) * kKB + hf * kHalfKeys, sv);
         ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        mbar_arrive(&s_free[q & 1]);
         // ---- masked, scaled scores and the block maximum of the row ----
         const int key0 = tree_blk ? 0 : (blk0 + i) * kKB;  // key (or node) of column 0
         const int kend = tree_blk ? N : ctx;
@@ -504,17 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st32(col, w);
           }
         }
-        // ---- P (bf16 hi and lo) -> TMEM, once its buffer's last product
-        // (two blocks ago; earlier segments are done) has completed ----
-        if (i >= 2 && !bad &&
-            !ptx::mbar_wait(&o_bar[(q - 2) & 1], (uint32_t)(((q - 2) >> 1) & 1)))
-          bad = true;
+        // ---- P (bf16 hi and lo) -> TMEM, over this block's S: every softmax
+        // thread has read its scores before the max exchange ----
         ptx::tc_fence_after();
         {
           uint32_t ph[16], pl[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], ph[e], pl[e]);
-          const uint32_t pc = tq + kColP + (uint32_t)(q & 1) * kKB + hf * 16;
+          const uint32_t pc = tq + kColSP + (uint32_t)(q & 1) * kKB + hf * 16;
           ptx::tmem_st16(pc, ph);
           ptx::tmem_st16(pc + kKB / 2, pl);
         }
