@@ -1018,9 +1018,9 @@ __global__ void __launch_bounds__(TcRes<NMAX>::threads, TcRes<NMAX>::ctas)
         ptx::tma_store_2d(&maps.state, a * 32, srow, st + a * (kStageBytes / 4));
       ptx::bulk_commit();
       ++n_stores;
-      // the next slab is loaded once the stores have read the stage: after
-      // the next tile's record wait, so that the issuing thread does not
-      // stall here while the stores drain
+      // the next slab is loaded once the stores have read the stage, at the
+      // next tile's top (so that the issuing thread does not stall here
+      // while the stores drain)
       if (it + 1 < count && nx.bq != bq) load_tab(nx);
     }
   }
