@@ -15,7 +15,8 @@
 // every node, links each node to its lowest-index matching child, finds the
 // accepted node by pointer jumping along those links (the reachable nodes
 // form one path, so the deepest is the largest index), and writes the
-// results.  The logits are read once, with 16-byte loads.
+// results.  The logits are read once, with 16-byte loads, four in flight
+// per thread.
 #include <stdint.h>
 
 #include "gdn_common.cuh"
@@ -99,7 +100,17 @@ __global__ void __launch_bounds__(kAccThreads) accept_walk_kernel(const AccArgs 
     const int nv = (hi - a0) >> 2, a1 = a0 + 4 * nv;
     for (int v = lo + tid; v < a0; v += kAccThreads) take(x, r[v], v);
     const float4 *r4 = reinterpret_cast<const float4 *>(r + a0);
-    for (int q = tid; q < nv; q += kAccThreads) take4(x, __ldcs(r4 + q), a0 + 4 * q);
+    // four 16-byte loads in flight per thread, visited in index order
+    int q = tid;
+    for (; q + 3 * kAccThreads < nv; q += 4 * kAccThreads) {
+      const float4 f0 = __ldcs(r4 + q), f1 = __ldcs(r4 + q + kAccThreads),
+                   f2 = __ldcs(r4 + q + 2 * kAccThreads), f3 = __ldcs(r4 + q + 3 * kAccThreads);
+      take4(x, f0, a0 + 4 * q);
+      take4(x, f1, a0 + 4 * (q + kAccThreads));
+      take4(x, f2, a0 + 4 * (q + 2 * kAccThreads));
+      take4(x, f3, a0 + 4 * (q + 3 * kAccThreads));
+    }
+    for (; q < nv; q += kAccThreads) take4(x, __ldcs(r4 + q), a0 + 4 * q);
     for (int v = a1 + tid; v < hi; v += kAccThreads) take(x, r[v], v);
     x = warp_best(x);
     if (lane == 0) red_v[warp] = x.v, red_i[warp] = x.i;
