@@ -11,8 +11,9 @@ with the step's inputs copied from pinned host memory and o copied back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lbx|reference]
-                       [--workload NAME] [--op verify|accept|ddtree|attn]
-`--op accept` times lbx_accept_walk (verify argmax + greedy acceptance walk)
+                       [--workload NAME] [--op verify|unfused|accept|ddtree|attn]
+`--op unfused` times lbx_tree_conv -> lbx_tree_deltanet (node states) ->
+lbx_tree_persist on --workload, `--op accept` times lbx_accept_walk (verify argmax + greedy acceptance walk)
 on a 5-request serving batch instead, `--op ddtree` lbx_ddtree_build, `--op
 attn` lbx_tree_attention on --attn-workload (each a separate JSON line of its
 own).
@@ -729,6 +730,132 @@ def run_attn(args):
     print(json.dumps(line))
 
 
+def run_unfused(args, w):
+    """Times the three unfused entry points chained on one stream --
+    lbx_tree_conv -> lbx_tree_deltanet (with per-node state snapshots) ->
+    lbx_tree_persist -- on --workload, each kernel between CUDA events, with
+    its own algorithmic bytes and roofline fraction; the snapshot write of
+    lbx_tree_deltanet (N states per head) dominates."""
+    import torch
+    from tree_verify_linear_gb300 import lbx
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lbx.load()
+    inp = make_inputs(w, seed=w.seed + 7919 * rank)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = {k: to_dev(v) for k, v in inp.items()}
+    cfg = lbx.cfg_of(w)
+    qkv = torch.empty((w.L, w.Bq, w.N, w.C), device=dev)
+    o = torch.empty((w.L, w.Bq, w.N, w.Hv, w.d), device=dev)
+    ns = torch.empty((w.L, w.Bq, w.N, w.Hv, w.d, w.d), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    calls = [
+        lambda: lbx.lbx_tree_conv(cfg, d["x"], d["conv_w"], d["conv_cache"], d["parent"],
+                                  d["slot"], qkv, status, stream),
+        lambda: lbx.lbx_tree_deltanet(cfg, qkv, d["a"], d["b"], d["state"], d["parent"],
+                                      d["slot"], o, ns, status, stream),
+        lambda: lbx.lbx_tree_persist(cfg, d["x"], ns, d["parent"], d["slot"], d["accepted"],
+                                     d["state"], d["conv_cache"], status, stream),
+    ]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    gpu_id = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid) if uuid else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for _ in range(args.warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    barrier(world)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler.mark(True)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            ev[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    per = [1e3 * sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+           for i in range(3)]
+    per = [max_over_ranks(x, world, dev) for x in per]
+    us = sum(per)
+    if rank != 0:
+        return
+    L, Bq, N, Hv, dd, C, K = w.L, w.Bq, w.N, w.Hv, w.d, w.C, w.K
+    slab = dd * dd * 4
+    alg = [
+        # conv: x, weights, the slots' cached rows, parents; qkv out
+        L * Bq * N * C * 2 + L * C * K * 2 + L * Bq * (K - 1) * C * 4 + Bq * N * 4
+        + L * Bq * N * C * 4,
+        # deltanet: qkv, gates, S0, parents; o and every node's state out
+        L * Bq * N * C * 4 + 2 * L * Bq * N * Hv * 2 + L * Bq * Hv * slab + Bq * N * 4
+        + L * Bq * N * Hv * dd * 4 + L * Bq * N * Hv * slab,
+        # persist: the accepted node's state in, the slot's state out, the conv
+        # window (at most K-1 rows read and written)
+        2 * L * Bq * Hv * slab + 2 * L * Bq * (K - 1) * C * 4 + Bq * N * 4 + 2 * Bq * 4,
+    ]
+    peak, peak_kind = read_peaks()
+    names = ("tree_conv_kernel", "gdn_step_kernel (unfused, node states)", "tree_persist_kernel")
+    kernels = {n: {"us": t, "algorithmic_bytes": a, "GB/s": a / (t / 1e6) / 1e9,
+                   "frac": a / (t / 1e6) / 1e9 / peak}
+               for n, t, a in zip(names, per, alg)}
+    import oracle  # CPU baseline leg only
+    cpu = None
+    if not args.no_cpu_baseline:
+        # layer 0 of every request: conv, every head's recurrence with node
+        # states, the conv window; scaled by L
+        t0 = time.time()
+        mask = np.zeros((L, Bq), np.uint8)
+        mask[0, :] = 1
+        q0 = oracle.tree_conv(w, inp, lb_mask=mask)
+        for b in range(Bq):
+            s0 = int(inp["slot"][b])
+            for h in range(Hv):
+                oracle.deltanet_head(N, w.Hk, Hv, dd, h, w.q_scale, oracle.FORM_PATH, q0[0, b],
+                                     inp["a"][0, b], inp["b"][0, b], inp["state"][0, s0, h],
+                                     inp["parent"][b], accepted=int(inp["accepted"][b]),
+                                     want_states=True)
+            oracle.persist_conv_lb(N, C, K, inp["x"][0, b], inp["conv_cache"][0, s0],
+                                   inp["parent"][b], inp["accepted"][b])
+        dt = time.time() - t0
+        cpu = {"value": 1e6 * dt * L, "unit": "us per step", "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of {L} (all requests and heads, node states), scaled by {L}"}
+    line = {
+        "metric": "us per unfused verify step (lbx_tree_conv + lbx_tree_deltanet with node "
+                  "states + lbx_tree_persist)",
+        "value": us, "unit": "us per step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": describe(w), "L": L, "Bq": Bq, "N": N, "Hk": w.Hk, "Hv": Hv,
+                   "d": dd, "K": K, "parallelism": f"replicas x{world}",
+                   "l2": "node states of one step > L2"},
+        "roofline": {"bound": "hbm", "achieved": kernels[names[1]]["GB/s"], "peak": peak,
+                     "unit": "GB/s", "frac": kernels[names[1]]["frac"], "peak_kind": peak_kind,
+                     "traffic": None, "algorithmic_bytes": alg[1], "kernel": names[1],
+                     "timed": "lbx_tree_deltanet call between CUDA events"},
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -738,21 +865,26 @@ def main():
     ap.add_argument("--workload", default="step27b", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("verify", "accept", "ddtree", "attn"), default="verify",
-                    help="verify: lbx_verify_step on --workload (the headline); accept: "
-                         "lbx_accept_walk on a serving batch; ddtree: lbx_ddtree_build; "
-                         "attn: lbx_tree_attention on --attn-workload")
+    ap.add_argument("--op", choices=("verify", "unfused", "accept", "ddtree", "attn"),
+                    default="verify",
+                    help="verify: lbx_verify_step on --workload (the headline); unfused: "
+                         "lbx_tree_conv -> lbx_tree_deltanet -> lbx_tree_persist on --workload; "
+                         "accept: lbx_accept_walk on a serving batch; ddtree: "
+                         "lbx_ddtree_build; attn: lbx_tree_attention on --attn-workload")
     ap.add_argument("--attn-workload", default="attn27b")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
-    if args.op in ("accept", "ddtree", "attn"):
+    if args.op in ("unfused", "accept", "ddtree", "attn"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               f"--op {args.op} times the library only; its oracle is the "
                               "cpu_baseline field"}))
             return
-        {"accept": run_accept, "ddtree": run_ddtree, "attn": run_attn}[args.op](args)
+        if args.op == "unfused":
+            run_unfused(args, w)
+        else:
+            {"accept": run_accept, "ddtree": run_ddtree, "attn": run_attn}[args.op](args)
         return
     if args.impl == "reference":
         run_reference(args, w)

@@ -94,14 +94,11 @@ __host__ __device__ inline StepLayout step_layout(int D, int R, int TC, int CG, 
   return Ly;
 }
 
-// Conv + SiLU of 8 consecutive channels c0..c0+7 of one node, whose window
-// rows are win[0..KK) (>= 0: an x row of this (layer, request); < 0: cache row
-// -1-w).  Tap KK-1 multiplies the node itself.  conv_w holds each channel's KK
-// taps contiguously, so the 8 channels' taps are 8*KK consecutive bf16.
+// The KK taps of 8 consecutive channels c0..c0+7 as fp32.  conv_w holds each
+// channel's KK taps contiguously, so the 8 channels' taps are 8*KK
+// consecutive bf16.
 template <int KK>
-__device__ __forceinline__ void conv8_k(float (&out)[8], const int *win, const uint16_t *x_lb,
-                                        int C, const uint16_t *w_l, const float *cache_s, int c0) {
-  float wt[8][KK];
+__device__ __forceinline__ void conv_taps(float (&wt)[8][KK], const uint16_t *w_l, int c0) {
   if (KK == 4 || KK == 2) {
     // 16*KK bytes from a 16-byte boundary: KK 16-byte loads
     uint32_t w32[4 * KK];
@@ -125,26 +122,58 @@ __device__ __forceinline__ void conv8_k(float (&out)[8], const int *win, const u
 #pragma unroll
       for (int t = 0; t < KK; ++t) wt[e][t] = bf2f(w_l[(size_t)(c0 + e) * KK + t]);
   }
-  float acc[8];
+}
+
+// Pre-activation conv of channels c0..c0+7 of one node, whose window rows are
+// win[0..KK) (>= 0: an x row of this (layer, request); < 0: cache row -1-w).
+// Tap KK-1 multiplies the node itself.
+template <int KK>
+__device__ __forceinline__ void conv_rows(float (&acc)[8], const float (&wt)[8][KK],
+                                          const int *win, const uint16_t *x_lb, int C,
+                                          const float *cache_s, int c0) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  // every window row's load is issued before the first product, so that the
+  // KK rows cost one memory round trip, not KK
+  uint4 lo[KK], hi[KK];
 #pragma unroll
   for (int j = 0; j < KK; ++j) {
     const int row = win[j];
-    float xv[8];
     if (row >= 0) {
-      unpack8(ldg_u4(x_lb + (size_t)row * C + c0), xv);
+      lo[j] = ldg_u4(x_lb + (size_t)row * C + c0);
+      hi[j] = make_uint4(0u, 0u, 0u, 0u);
     } else {
       // coherent loads: the fused kernel rewrites the cache after every
       // reader of a row has finished with it
-      const float4 *cp = reinterpret_cast<const float4 *>(cache_s + (size_t)(-1 - row) * C + c0);
-      const float4 lo = cp[0], hi = cp[1];
-      xv[0] = lo.x, xv[1] = lo.y, xv[2] = lo.z, xv[3] = lo.w;
-      xv[4] = hi.x, xv[5] = hi.y, xv[6] = hi.z, xv[7] = hi.w;
+      const uint4 *cp = reinterpret_cast<const uint4 *>(cache_s + (size_t)(-1 - row) * C + c0);
+      lo[j] = cp[0];
+      hi[j] = cp[1];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KK; ++j) {
+    float xv[8];
+    if (win[j] >= 0) {
+      unpack8(lo[j], xv);
+    } else {
+      xv[0] = __uint_as_float(lo[j].x), xv[1] = __uint_as_float(lo[j].y);
+      xv[2] = __uint_as_float(lo[j].z), xv[3] = __uint_as_float(lo[j].w);
+      xv[4] = __uint_as_float(hi[j].x), xv[5] = __uint_as_float(hi[j].y);
+      xv[6] = __uint_as_float(hi[j].z), xv[7] = __uint_as_float(hi[j].w);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = fmaf(wt[e][KK - 1 - j], xv[e], acc[e]);
   }
+}
+
+// Conv + SiLU of 8 consecutive channels c0..c0+7 of one node.
+template <int KK>
+__device__ __forceinline__ void conv8_k(float (&out)[8], const int *win, const uint16_t *x_lb,
+                                        int C, const uint16_t *w_l, const float *cache_s, int c0) {
+  float wt[8][KK];
+  conv_taps<KK>(wt, w_l, c0);
+  float acc[8];
+  conv_rows<KK>(acc, wt, win, x_lb, C, cache_s, c0);
 #pragma unroll
   for (int e = 0; e < 8; ++e) out[e] = silu(acc[e]);
 }
