@@ -575,20 +575,40 @@ __global__ void __launch_bounds__(kThreads) gdn_step_kernel(const StepArgs A) {
     // ---- 8. state epilogues: S_t rows = gamma_t S0 + sum_{j on path(t)} g(j->t) delta_j k_j^T
     // Target path of node t: t itself with coefficient 1, then its parent-path
     // list with coefficients pg * a_t; gamma_t = gam[t] * a_t.
+    // A thread always owns column chunk q = tid % DQ of rows r0, r0 + RS, ...
+    // (kThreads is a multiple of DQ), so each path term's k chunk is read
+    // from shared memory once and applied to all the thread's rows; the
+    // deltas are warp broadcasts.  Per element the sum is formed in the
+    // same order as above (S0 term, the node's own term, then its path).
     auto state_rows = [&](int t, float *dst_base, bool to_smem) {
+      static_assert(kThreads % DQ == 0 && (R * DQ) % kThreads == 0, "state row split");
+      constexpr int M = R * DQ / kThreads, RS = kThreads / DQ;
+      const int q = tid % DQ, r0 = tid / DQ;
       const float gt = gam[t] * an[t];
       const float at = an[t];
-      for (int idx = tid; idx < R * DQ; idx += kThreads) {
-        const int r = idx / DQ, q = idx % DQ;
-        const int sidx = r * DQ + swz(q, r);
-        float4 acc = f4_scale(gt, S0s[sidx]);
-        f4_fma(acc, DEL[t * R + r], KQ[t * DQ + swz(q, t)]);
-        for (int e = off[t]; e < off[t + 1]; ++e) {
-          const int j = pj[e];
-          f4_fma(acc, pg[e] * at * DEL[j * R + r], KQ[j * DQ + swz(q, j)]);
-        }
-        if (to_smem) S0s[sidx] = acc;
-        else stg_f4(dst_base + (size_t)r * D + 4 * q, acc);
+      float4 acc[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int r = r0 + m * RS;
+        acc[m] = f4_scale(gt, S0s[r * DQ + swz(q, r)]);
+      }
+      {
+        const float4 kt = KQ[t * DQ + swz(q, t)];
+#pragma unroll
+        for (int m = 0; m < M; ++m) f4_fma(acc[m], DEL[t * R + r0 + m * RS], kt);
+      }
+      for (int e = off[t]; e < off[t + 1]; ++e) {
+        const int j = pj[e];
+        const float c = pg[e] * at;
+        const float4 kj = KQ[j * DQ + swz(q, j)];
+#pragma unroll
+        for (int m = 0; m < M; ++m) f4_fma(acc[m], c * DEL[j * R + r0 + m * RS], kj);
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int r = r0 + m * RS;
+        if (to_smem) S0s[r * DQ + swz(q, r)] = acc[m];
+        else stg_f4(dst_base + (size_t)r * D + 4 * q, acc[m]);
       }
     };
     if (PERSIST) {
