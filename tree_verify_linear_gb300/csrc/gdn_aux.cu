@@ -37,7 +37,26 @@ __device__ __forceinline__ void conv_group(const ConvArgs &A, const int *win, in
     const bool on = act && i < N;
     float v8[8];
     if (on) {
-      conv_rows<KK>(v8, wt, win + i * LBX_MAX_CONV_WIDTH, x_lb, C, cache_s, c0);
+      const int *wi = win + i * LBX_MAX_CONV_WIDTH;
+      // cache rows are a suffix of the window, so a deepest entry that is an
+      // x row means every row is one: K bf16 loads, no fp32 halves, no
+      // per-row select (same products in the same order as conv_rows)
+      if (wi[KK - 1] >= 0) {
+        uint4 xr[KK];
+#pragma unroll
+        for (int j = 0; j < KK; ++j) xr[j] = ldg_u4(x_lb + (size_t)wi[j] * C + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v8[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < KK; ++j) {
+          float xv[8];
+          unpack8(xr[j], xv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v8[e] = fmaf(wt[e][KK - 1 - j], xv[e], v8[e]);
+        }
+      } else {
+        conv_rows<KK>(v8, wt, wi, x_lb, C, cache_s, c0);
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) v8[e] = silu_fast(v8[e]);
     } else {
