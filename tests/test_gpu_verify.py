@@ -3,12 +3,14 @@ oracle, on the seeded workloads at full size and on edge cases.  Calls go
 through the C ABI (ctypes binding)."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from tree_verify_linear_gb300 import lbx
 from tree_verify_linear_gb300.inputs import WORKLOADS, Workload, bf16_bits, make_inputs
 
-from gpu_util import O_TOL, STATE_TOL, check_verify, counters_cleared, run_verify
+from gpu_util import (O_TOL, STATE_TOL, check_verify, counters_cleared, dev_inputs,
+                      run_verify)
 
 pytestmark = pytest.mark.gpu
 
@@ -130,6 +132,45 @@ def test_chunked_chain_lengths(N, acc):
     o, st, cc, status, _ = run_verify(w, inp, mode=lbx.LBX_MODE_CHUNKED)
     assert status == 0
     check_verify(w, inp, o, st, cc, form=oracle.FORM_SEQUENTIAL)
+
+
+def _at_16_past_32(t: torch.Tensor) -> torch.Tensor:
+    """A copy of t whose data starts 16 bytes past a 32-byte boundary: the
+    weakest alignment the header allows for every array."""
+    es = t.element_size()
+    buf = torch.empty(t.numel() + 64 // es, dtype=t.dtype, device=t.device)
+    k = next(k for k in range(64 // es) if (buf.data_ptr() + k * es) % 32 == 16)
+    v = buf[k:k + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("mode,kw", [
+    (lbx.LBX_MODE_CHUNKED, dict(N=100, tree="chain", accepted="last", Hk=2, Hv=2)),
+    (lbx.LBX_MODE_TREE, dict(N=22, Hk=2, Hv=4)),
+    (lbx.LBX_MODE_TREE_CUDA_CORES, dict(N=22, Hk=2, Hv=4)),
+])
+def test_arrays_16_bytes_past_a_32_byte_boundary(mode, kw):
+    """Every array 16-byte aligned but not 32-byte aligned (the header asks
+    for 16): the chunked tensor-core path, the tree tensor-core path and the
+    CUDA-core tree kernel give the same outputs, bit for bit, as with
+    aligned arrays."""
+    w = small(d=128, seed=3100 + mode, **kw)
+    inp = make_inputs(w)
+    ref = run_verify(w, inp, mode=mode)
+    d = {k: _at_16_past_32(v) for k, v in dev_inputs(inp).items()}
+    cfg = lbx.cfg_of(w, mode)
+    o = _at_16_past_32(torch.full((w.L, w.Bq, w.N, w.Hv, w.d), float("nan"), device="cuda"))
+    ws = lbx.new_workspace(cfg)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lbx.lbx_verify_step(cfg, d["x"], d["conv_w"], d["a"], d["b"], d["parent"], d["slot"],
+                        d["accepted"], d["state"], d["conv_cache"], o, ws, status)
+    torch.cuda.synchronize()
+    assert ref[3] == 0 and int(status.item()) == 0
+    assert o.cpu().numpy().tobytes() == ref[0].tobytes()
+    assert d["state"].cpu().numpy().tobytes() == ref[1].tobytes()
+    assert d["conv_cache"].cpu().numpy().tobytes() == ref[2].tobytes()
 
 
 def test_tree_and_chunked_modes_agree_on_a_chain():

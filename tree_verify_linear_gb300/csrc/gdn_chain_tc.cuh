@@ -674,11 +674,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
           float d[32];
           ptx::tmem_ld32(tq + Ly::cA1 + k0, d);
           ptx::tmem_wait_ld();
+          // 16-byte stores: the state is only required to be 16-byte aligned
           if (to_global)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              stg_v8(srow + k0 + 8 * q, d[8 * q], d[8 * q + 1], d[8 * q + 2], d[8 * q + 3],
-                     d[8 * q + 4], d[8 * q + 5], d[8 * q + 6], d[8 * q + 7]);
+            for (int q = 0; q < 8; ++q)
+              stg_f4(srow + k0 + 4 * q, make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]));
           if (to_stage)
 #pragma unroll
             for (int q = 0; q < 8; ++q)

@@ -408,14 +408,6 @@ __device__ __forceinline__ void conv8_staged_tree(float (&out)[8], const int4 w4
   for (int e = 0; e < 8; ++e) out[e] = silu_fast(acc[e]);
 }
 
-// 32-byte store of 8 floats (32-byte aligned address).
-__device__ __forceinline__ void stg_v8(float *p, float v0, float v1, float v2, float v3, float v4,
-                                       float v5, float v6, float v7) {
-  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v0),
-               "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7)
-               : "memory");
-}
-
 // New conv-window entries of channel gc, from global memory: row rr takes
 // src[rr] (>= 0: x row of the request; < 0: old cache row -1-src).  Every old
 // value is read before any is written (the window is updated in place).
