@@ -846,7 +846,8 @@ def run_unfused(args, w):
                    "l2": "node states of one step > L2"},
         "roofline": {"bound": "hbm", "achieved": kernels[names[1]]["GB/s"], "peak": peak,
                      "unit": "GB/s", "frac": kernels[names[1]]["frac"], "peak_kind": peak_kind,
-                     "traffic": None, "algorithmic_bytes": alg[1], "kernel": names[1],
+                     "traffic": recorded_traffic(f"{w.name}_unfused"),
+                     "algorithmic_bytes": alg[1], "kernel": names[1],
                      "timed": "lbx_tree_deltanet call between CUDA events"},
         "kernels": kernels,
         "cpu_baseline": cpu,
