@@ -794,6 +794,37 @@ def run_unfused(args, w):
            for i in range(3)]
     per = [max_over_ranks(x, world, dev) for x in per]
     us = sum(per)
+
+    # ---- end to end: the step's inputs from pinned host memory and o back,
+    # inside the timed region (states, caches and snapshots stay resident) ----
+    names_in = ("x", "a", "b", "parent", "slot", "accepted")
+    host = {k: d[k].cpu().pin_memory() for k in names_in}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k in names_in:
+            d[k].copy_(host[k], non_blocking=True)
+        for c in calls:
+            c()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    e2e_us = max_over_ranks(1e3 * e0.elapsed_time(e1) / e2e_steps, world, dev)
     if rank != 0:
         return
     L, Bq, N, Hv, dd, C, K = w.L, w.Bq, w.N, w.Hv, w.d, w.C, w.K
@@ -851,6 +882,8 @@ def run_unfused(args, w):
                      "timed": "lbx_tree_deltanet call between CUDA events"},
         "kernels": kernels,
         "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us per step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(),
     }
